@@ -1,0 +1,371 @@
+"""Benchmark of the KDA decode / speculative-verify step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload NAME]
+
+A step is one call of the library (one kernel launch) over one batch of the
+workload: by default decode_b256_h32 (B=256 requests, H=32 heads, 8192
+(request, head) items, 1 GiB of FP32 state pages read + written per step).
+Inputs are seeded synthetic tensors resident in HBM before the timed region.
+The state pages one step touches (512 MiB) exceed the 129 MB L2, so no L2
+flush is inserted between steps.
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own batch of
+the same shape on its own GPU (weak scaling, no collective on the data path);
+timing is the max over ranks.
+
+--impl reference times the CPU oracle on the host cores (the only comparison
+implementation that exists for this path), on a bounded sample of the same
+workload; rank 0 alone runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA decode (req,head) items/s + achieved HBM GB/s vs ~8 TB/s at B=256,H=32"
+UNIT = "items/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCE = os.path.join(ROOT, "linear_attention_recurrent_kda_gb300", "csrc",
+                             "kda_step.cu")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", f"kda_step_{workload}.ncu.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+    except Exception:
+        return None
+    if p.get("source_sha256") != kernel_sha():
+        return None
+    return p.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (100 ms)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.samples:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        window = [p for ts, p in rows if t0 <= ts <= t1]
+        if not window:
+            return None
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in window if num(p[1]) is not None]
+        mx = [num(p[2]) for p in window if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i - 5] for p in window for i in range(5, 9)
+                          if p[i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(window)}
+
+
+def run_reference(args, workload):
+    """The CPU oracle timed on the host cores over a bounded item sample."""
+    import numpy as np
+    import oracle
+    from linear_attention_recurrent_kda_gb300.workloads import make_inputs
+    from tests.hostdata import to_oracle
+    inp = to_oracle(make_inputs(workload))
+    threads = oracle.max_threads()
+    rng = np.random.default_rng(0)
+    order = rng.permutation(workload.items).astype(np.int32)
+    t = time.perf_counter()
+    oracle.run(inp, mode="f32", items=np.sort(order[:64]), in_place=True,
+               threads=threads)
+    per_item = (time.perf_counter() - t) / 64
+    # size each step so the whole run stays near one minute of CPU time
+    n = int(max(16, min(1024, 60.0 / (max(args.steps, 1) * per_item))))
+    items = np.sort(order[:n])
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.run(inp, mode="f32", items=items, in_place=True, threads=threads)
+        times.append(time.perf_counter() - t)
+    per_step = sum(times) / len(times)
+    value = n / per_step
+    sample = (f"{n} of {workload.items} items per step (seeded), full per-item "
+              f"step incl. state page read/write, {threads} OpenMP threads")
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3 * workload.items / n,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload.name, "batch": workload.batch,
+                   "heads": workload.heads, "tokens": workload.tokens,
+                   "items": workload.items},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline(workload, budget_s=12.0):
+    import numpy as np
+    import oracle
+    from linear_attention_recurrent_kda_gb300.workloads import make_inputs
+    from tests.hostdata import to_oracle
+    inp = to_oracle(make_inputs(workload))
+    threads = oracle.max_threads()
+    rng = np.random.default_rng(1)
+    n = min(workload.items, 1024)
+    items = np.sort(rng.choice(workload.items, size=n, replace=False)).astype(np.int32)
+    done, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and done < 64 * n:
+        oracle.run(inp, mode="f32", items=items, in_place=True, threads=threads)
+        done += n
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{done} items ({n}-item seeded sample of {workload.name}, "
+                      f"repeated) in {dt:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="decode_b256_h32")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from linear_attention_recurrent_kda_gb300.workloads import WORKLOADS
+    workload = WORKLOADS[args.workload]
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, workload)), flush=True)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    from linear_attention_recurrent_kda_gb300.accounting import step_bytes
+    from linear_attention_recurrent_kda_gb300.api import step_from_inputs
+    from linear_attention_recurrent_kda_gb300.workloads import make_inputs
+
+    w = workload.with_(seed=workload.seed + 7919 * rank)
+    host = make_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    B, H, T = w.batch, w.heads, w.tokens
+    out = torch.empty((B * T, H * 128), dtype=torch.bfloat16, device=dev)
+    rec_u = rec_kg = None
+    if w.record:
+        rec_u = torch.empty((B, H, T, 128), dtype=torch.float32, device=dev)
+        rec_kg = torch.empty((B, H, T, 256), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    step = step_from_inputs(d, out, rec_u=rec_u, rec_kg=rec_kg)
+    nbytes = step_bytes(w, host)
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step(stream)
+        stream.synchronize()
+        # extra untimed soak so clock samples exist around a short timed region
+        t_soak = time.time()
+        soak = 0
+        while time.time() - t_soak < 1.0:
+            for _ in range(200):
+                step(stream)
+            stream.synchronize()
+            soak += 200
+
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize(dev)
+        t_host0 = time.time()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step(stream)
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        t_host1 = time.time()
+    sampler.stop()
+    total_ms = t0.elapsed_time(t1)
+    kern_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+    ms_step = total_ms / args.steps
+    if pg is not None:
+        t = torch.tensor([ms_step, kern_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_step, kern_ms = float(t[0]), float(t[1])
+    clocks = sampler.summary(t_host0 - 0.15, t_host1 + 0.15)
+    clock_window = "timed"
+    if clocks is None:
+        clocks = sampler.summary(t_soak, t_host1 + 0.15)
+        clock_window = "soak+timed (timed region shorter than the 100 ms sample period)"
+
+    # ---- end to end: pinned host inputs -> device, the call, output -> host
+    per_step_in = ["x", "f_a", "beta", "gate", "slots"] + (["accepted"] if T > 1 else [])
+    pinned = {k: host[k].pin_memory() for k in per_step_in}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in per_step_in)
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_steps = max(1, min(args.steps, 500))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for k in per_step_in:
+                d[k].copy_(pinned[k], non_blocking=True)
+            step(stream)
+            out_host.copy_(out, non_blocking=True)
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for k in per_step_in:
+                d[k].copy_(pinned[k], non_blocking=True)
+            step(stream)
+            out_host.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if pg is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+
+    items = w.items * world
+    value = items / (ms_step * 1e-3)
+    peak, peak_kind = measured_peak()
+    achieved = nbytes["total"] / (kern_ms * 1e-3) / 1e9
+    state_gbs = nbytes["state"] / (kern_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(w.name if rank == 0 else workload.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload.name, "batch": B, "heads": H, "tokens": T,
+                   "items_per_gpu": w.items, "state_io": "fp32 pages, bf16 activations",
+                   "l2": "inputs larger than L2: 512 MiB of state pages touched per "
+                         "step vs 129 MB L2; no flush",
+                   "parallelism": f"replica x{world} (independent batches)"},
+        "tokens_per_s": items * T / (ms_step * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": nbytes["total"],
+                     "state_bytes_per_launch": nbytes["state"],
+                     "state_gbs": state_gbs, "state_frac": state_gbs / peak,
+                     "kernel_ms": kern_ms},
+        "clocks": dict(clocks or {}, window=clock_window),
+        "e2e": {"value": items / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(workload)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

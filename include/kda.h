@@ -1,0 +1,147 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) KDA decode / speculative-verify step.
+ *
+ * The operation is the one defined by the vLLM API page
+ *   "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.kda.wide"
+ * (class KdaWide: the constructor's validation, `kernel`, and the helpers
+ * `silu`, `decay`, `quad_sum`).  For every (request r, head h) item one call:
+ *
+ *   1. resolves the item's slots (decode: slot = conv slot = slots[r], window
+ *      offset 0; verify: slot = slots[r, accepted[r]-1], conv slot =
+ *      slots[r, 0], window offset accepted[r]-1); slot <= 0 marks padding:
+ *      the item's output rows are BF16 zeros and nothing else is written;
+ *   2. runs the 4-tap causal depthwise convolution over the three cached taps
+ *      and the new inputs (plus optional bias), SiLU, BF16 rounding (q, k, v);
+ *   3. computes the low-rank gate raw_g = BF16(f_b[h] . f_a[row]) and the decay
+ *      exp(lower_bound * sigmoid(exp(A_log[h]) * (raw_g + dt_bias)));
+ *   4. beta = sigmoid(beta_raw); L2-normalises q (times scale) and k;
+ *   5. applies the per-key-decayed delta rule to the 128x128 FP32 state page
+ *      [value row i][key j]:  S *= d (per key);  u = (v - S k) * beta;
+ *      S += u k^T;  o = BF16(S q);  and writes the page after every token to
+ *      slot (decode) or slots[r, t] when > 0 (verify), or, in record mode,
+ *      writes the records instead of any state;
+ *   6. writes the new conv window [tap1, tap2, x_0 .. x_{T-1}];
+ *   7. out = BF16(((o * rsqrt(mean(o^2) + eps)) * norm_weight) * sigmoid(gate)).
+ *
+ * Sizes fixed by the method: dk = dv = 128 and gate rank 128, conv kernel 4.
+ * Arithmetic: FP32 with BF16 rounding of q, k, v, raw_g and o; exp is
+ * 2^(x*log2 e) on the hardware's approximate exp2, division / square root /
+ * reciprocal are the hardware's approximate (full-range) instructions, the
+ * gate projection runs on tensor cores with FP32 accumulation.  Only FP32
+ * reduction order differs from a sequential evaluation.
+ *
+ * Ownership and threading: the caller owns every buffer; every pointer is a
+ * DEVICE pointer of the current device.  The library allocates nothing,
+ * never synchronises, and enqueues exactly one kernel on `stream` per call.
+ * Calls are reentrant; two calls that write the same pool regions must be
+ * ordered by the caller (same stream or events).
+ *
+ * Aliasing contract: within one call, the state pages and conv rows touched
+ * by different requests must be distinct (distinct slots per request).  An
+ * item may write the page it read (same slot): its read completes first.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_ABI_VERSION 1
+#define KDA_DK 128
+#define KDA_MAX_TOKENS 8
+
+/* Host-side return codes (nothing is launched unless KDA_SUCCESS). */
+enum {
+  KDA_SUCCESS = 0,
+  KDA_ERR_NULL_ARGS = 1,      /* args == NULL                                  */
+  KDA_ERR_TOKENS = 2,         /* tokens outside 1..8 (KdaWide.__init__), or    */
+                              /* kda_decode with tokens != 1, kda_verify == 1  */
+  KDA_ERR_GATE_MODE = 3,      /* gate_mode not 0|1 (KdaWide.__init__)          */
+  KDA_ERR_RECORD = 4,         /* record with tokens == 1 (KdaWide.__init__)    */
+  KDA_ERR_NULL_POINTER = 5,   /* a required pointer is NULL                    */
+  KDA_ERR_CONV_WIDTH = 6,     /* conv_width < tokens + 2, or too wide to stage */
+  KDA_ERR_ALIGNMENT = 7,      /* a pointer breaks its alignment rule (below)   */
+  KDA_ERR_SHAPE = 8,          /* negative sizes, num_slots < 1, slot_cols <    */
+                              /* tokens, or an item count beyond 2^31-1        */
+  KDA_ERR_DEVICE = 9,         /* no usable device, or not an sm_103 device     */
+  KDA_ERR_LAUNCH = 10         /* the kernel launch failed (CUDA error)         */
+};
+
+/* Device-side error flags, OR-ed into *err when err != NULL.  An item that
+ * raises one is handled like padding (zero output rows, nothing written). */
+enum {
+  KDA_DEVERR_SLOT = 1,        /* slot, conv slot or a write target >= num_slots,
+                                 or a conv slot <= 0 on a live verify item     */
+  KDA_DEVERR_ACCEPTED = 2,    /* accepted[r] outside 1..tokens                 */
+  KDA_DEVERR_TIMEOUT = 4      /* an on-chip copy wait ran out (the kernel      */
+                              /* stopped early; outputs are incomplete)        */
+};
+
+/* Arguments of one step.  Layouts are row-major; dim = heads * 128.
+ * Alignment: state, f_a, f_b, x, gate and conv_state 16 bytes; the other BF16
+ * arrays 2 bytes, FP32/int32 arrays 4 bytes. */
+typedef struct kda_args {
+  int32_t batch;       /* B requests (0 is a no-op)                          */
+  int32_t heads;       /* H heads (0 is a no-op)                             */
+  int32_t tokens;      /* T: 1 = decode, 2..8 = verify                       */
+  int32_t num_slots;   /* slots in both pools; slot 0 is the null slot       */
+  int32_t conv_width;  /* W columns per conv channel row, >= T + 2           */
+  int32_t slot_cols;   /* row stride of `slots` in verify, >= T (decode: 1)  */
+  int32_t gate_mode;   /* 0: one FP32 chain over the rank; 1: four chains    */
+                       /* over rank quarters, then 0 + (((c0+c1)+c2)+c3)     */
+  int32_t has_bias;    /* conv bias present                                  */
+  int32_t record;      /* record ("RecoverSSM verify") mode, T > 1 only      */
+  int32_t use_pdl;     /* launch with programmatic dependent launch; the     */
+                       /* state/conv pools, slots and accepted are then read */
+                       /* before the preceding kernel finishes               */
+
+  const void *x;            /* bf16 [B*T, 3*dim]  q | k | v column blocks    */
+  const void *conv_weight;  /* bf16 [3, 4, dim]   (part, tap, channel)       */
+  const void *conv_bias;    /* bf16 [3*dim] (has_bias) else ignored          */
+  const void *f_a;          /* bf16 [B*T, 128]                               */
+  const void *f_b;          /* bf16 [dim, 128]    (feature, rank)            */
+  const void *beta;         /* bf16 [B*T, H]      raw logits                 */
+  const void *gate;         /* bf16 [B*T, dim]    output gate logits         */
+  const void *norm_weight;  /* bf16 [128]         shared by all heads        */
+  const float *a_log;       /* f32  [H]                                      */
+  const float *dt_bias;     /* f32  [dim]                                    */
+  const int32_t *slots;     /* i32  [B] (decode) or [B, slot_cols] (verify)  */
+  const int32_t *accepted;  /* i32  [B] (verify), ignored by decode          */
+
+  void *conv_state;         /* bf16 [num_slots, 3*dim, W]        in/out      */
+  float *state;             /* f32  [num_slots, H, 128, 128]     in/out      */
+  void *output;             /* bf16 [B*T, dim]                   out         */
+  float *rec_u;             /* f32  [B, H, T, 128]  record only, else NULL   */
+  void *rec_kg;             /* bf16 [B, H, T, 256]  record only: k | raw_g   */
+
+  float lower_bound;        /* decay lower bound (e.g. -5)                   */
+  float scale;              /* q scale (e.g. 128^-0.5)                       */
+  float eps;                /* RMSNorm epsilon (the L2 norms use 1e-6)       */
+
+  int32_t *err;             /* optional device word for KDA_DEVERR_* flags   */
+  void *dbg;                /* optional bf16 [B, H, T, 4, 128]: q, k, v      */
+                            /* (after SiLU, before the norm) and raw_g, as   */
+                            /* this call rounded them; for parity checks     */
+} kda_args;
+
+/* One decode step (tokens == 1) on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream).  Returns KDA_SUCCESS or a KDA_ERR_* code. */
+int kda_decode(const kda_args *args, void *stream);
+
+/* One speculative-verify step (tokens 2..8, record optional) on `stream`. */
+int kda_verify(const kda_args *args, void *stream);
+
+/* Static description of a return code (never NULL). */
+const char *kda_strerror(int code);
+
+/* KDA_ABI_VERSION of the loaded library. */
+int kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */

@@ -1,0 +1,63 @@
+"""Build the in-tree CUDA library ``libkda_gb300.so`` for sm_103a.
+
+One translation unit (csrc/kda_step.cu) compiled by nvcc with a single
+``-gencode arch=compute_103a,code=sm_103a``; the result sits next to this file
+and is loaded by ``linear_attention_recurrent_kda_gb300.lib``.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import tempfile
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+ROOT = os.path.dirname(HERE)
+INCLUDE = os.path.join(ROOT, "include")
+LIB_PATH = os.path.join(HERE, "libkda_gb300.so")
+SOURCES = [os.path.join(CSRC, "kda_step.cu")]
+HEADERS = [os.path.join(INCLUDE, "kda.h")]
+
+NVCC_FLAGS = [
+    "-gencode", "arch=compute_103a,code=sm_103a",
+    "-O3", "-lineinfo", "-std=c++17",
+    "-shared", "-Xcompiler", "-fPIC",
+]
+
+
+def nvcc() -> str:
+    cand = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(cand):
+        raise RuntimeError("nvcc not found")
+    return cand
+
+
+def is_stale() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return True
+    t = os.path.getmtime(LIB_PATH)
+    return any(os.path.getmtime(s) > t for s in SOURCES + HEADERS)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the library if missing or older than its sources."""
+    if not force and not is_stale():
+        return LIB_PATH
+    with tempfile.TemporaryDirectory() as tmp:
+        out = os.path.join(tmp, "libkda_gb300.so")
+        cmd = [nvcc()] + NVCC_FLAGS + ["-I", INCLUDE, "-o", out] + SOURCES
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
+        if verbose:
+            print(res.stdout + res.stderr)
+        os.replace(out, LIB_PATH)
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    import sys
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

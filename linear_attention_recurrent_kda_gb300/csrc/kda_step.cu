@@ -1,0 +1,1010 @@
+// KDA decode / speculative-verify step for GB300 (sm_103a).
+//
+// Method: vLLM API page
+//   "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.kda.wide"
+// (class KdaWide: `kernel`, `silu`, `decay`, `quad_sum`); the C ABI and the
+// step it runs are described in include/kda.h.
+//
+// Design (GB300-first; the page's one-CTA-per-item kernel is prior art):
+//   * Persistent kernel, one CTA per SM.  Each CTA owns a contiguous range of
+//     items in head-major order (item = h * batch + r), so the per-head
+//     constants (f_b tensor-core fragments, conv weights, dt_bias) stay in
+//     registers across its items.
+//   * Warp 8 is the producer: per item it resolves the slots, loads the
+//     scalar inputs (beta, targets) into an item descriptor and stages the
+//     64 KiB FP32 state page plus the item's conv rows, x, gate and f_a rows
+//     into a shared-memory ring of 2-3 stages with cp.async.bulk (TMA bulk
+//     copies) signalling an mbarrier.  It runs 2-3 items ahead, so the HBM
+//     read of later pages overlaps the compute of the current one.
+//   * Warps 0-7 are consumers.  Front: conv + SiLU (threads own channels),
+//     gate projection on tensor cores (mma.sync m16n8k16 BF16, FP32 accumulate,
+//     warp w owns features 16w..16w+15), decay, beta, L2 norms.  Recurrence:
+//     thread (g = tid/8, l = tid%8) holds keys {32c + 4l + e} of value rows
+//     g, g+32, g+64, g+96 in registers (64 floats), packed FP32 FMAs
+//     (f32x2), row reductions as an 8-lane reduce-scatter.  The updated page
+//     goes straight from registers to HBM with 16-byte streaming stores.
+//   * Every wait is bounded (wall clock) and reports KDA_DEVERR_TIMEOUT.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+constexpr int kDk = 128;                    // dk = dv = gate rank
+constexpr int kConsumers = 256;             // warps 0-7
+constexpr int kThreads = kConsumers + 32;   // + producer warp 8
+constexpr uint32_t kPageBytes = kDk * kDk * 4;
+constexpr int kMaxStages = 3;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kLive = 0, kPad = 1, kError = 2;
+
+struct __align__(16) ItemDesc {
+  int32_t status;
+  int32_t slot;
+  int32_t conv_slot;
+  int32_t offset;
+  int32_t target[KDA_MAX_TOKENS];
+  uint16_t beta_bits[KDA_MAX_TOKENS];
+};
+
+struct Params {
+  int32_t batch, heads, num_slots, conv_width, slot_cols, gate_mode, has_bias;
+  int32_t items, stages;
+  uint32_t stage_bytes, conv_off, x_off, gate_off, fa_off;
+  uint32_t bar_off, desc_off, front_off;
+  const __nv_bfloat16 *x, *conv_weight, *conv_bias, *f_a, *f_b, *beta, *gate,
+      *norm_weight;
+  const float *a_log, *dt_bias;
+  const int32_t *slots, *accepted;
+  __nv_bfloat16 *conv_state;
+  float *state;
+  __nv_bfloat16 *output;
+  float *rec_u;
+  __nv_bfloat16 *rec_kg;
+  float lower_bound, scale, eps;
+  int32_t *err;
+  __nv_bfloat16 *dbg;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(
+                   smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for the phase of `parity` to complete; false after kWaitLimitNs of
+// wall clock (or 2^30 polls, whichever first).
+__device__ __noinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// TMA bulk copy global -> this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src,
+                                              uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+// Barrier over the 256 consumer threads that also ORs a predicate.
+__device__ __forceinline__ bool consumer_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// m16n8k16 BF16 tensor-core MMA, FP32 accumulate in place.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4],
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------- the page's approximate math
+// exp(x) = 2^(x log2 e) on the approximate exp2 instruction; division, square
+// root and reciprocal on the approximate full-range instructions.
+
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float exp_approx(float x) {
+  return exp2_approx(__fmul_rn(x, 1.4426950408889634f));
+}
+__device__ __forceinline__ float div_full(float a, float b) {
+  float y;
+  asm("div.full.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+  return y;
+}
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float y;
+  asm("sqrt.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float sigmoid_approx(float z) {
+  return div_full(1.0f, __fadd_rn(1.0f, exp_approx(-z)));
+}
+// KdaWide.silu before its BF16 rounding.
+__device__ __forceinline__ float silu_approx(float a) {
+  return div_full(a, __fadd_rn(1.0f, exp_approx(-a)));
+}
+__device__ __forceinline__ float bf16_round(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, s));
+  return v;
+}
+
+// Sum over the 8 lanes of a row group of four partial sums (one per value row
+// m = 0..3); returns the total of row (lane >> 1) & 3.
+__device__ __forceinline__ float reduce_scatter8(const float (&x)[4], int l) {
+  const bool hi2 = (l >> 2) & 1;
+  float keep0 = hi2 ? x[2] : x[0], keep1 = hi2 ? x[3] : x[1];
+  const float send0 = hi2 ? x[0] : x[2], send1 = hi2 ? x[1] : x[3];
+  keep0 = __fadd_rn(keep0, __shfl_xor_sync(0xffffffffu, send0, 4));
+  keep1 = __fadd_rn(keep1, __shfl_xor_sync(0xffffffffu, send1, 4));
+  const bool hi1 = (l >> 1) & 1;
+  float keep = hi1 ? keep1 : keep0;
+  const float send = hi1 ? keep0 : keep1;
+  keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+  keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, keep, 1));
+  return keep;
+}
+
+// ----------------------------------------------------------------- producer
+
+template <int T, bool RECORD>
+__device__ __forceinline__ int resolve_item(const Params &p, int n, ItemDesc &d) {
+  const int h = n / p.batch;
+  const int r = n - h * p.batch;
+  (void)h;
+  int s, cs, off;
+  int flags = 0;
+  if (T == 1) {
+    s = __ldg(p.slots + r);
+    cs = s;
+    off = 0;
+  } else {
+    const int a = __ldg(p.accepted + r);
+    if (a < 1 || a > T) {
+      d.status = kError;
+      return KDA_DEVERR_ACCEPTED;
+    }
+    off = a - 1;
+    s = __ldg(p.slots + static_cast<int64_t>(r) * p.slot_cols + off);
+    cs = __ldg(p.slots + static_cast<int64_t>(r) * p.slot_cols);
+  }
+  d.slot = s;
+  d.conv_slot = cs;
+  d.offset = off;
+  if (s <= 0) {
+    d.status = kPad;
+    return 0;
+  }
+  if (s >= p.num_slots || cs <= 0 || cs >= p.num_slots) flags |= KDA_DEVERR_SLOT;
+  if (T > 1 && !RECORD) {
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      const int tg = __ldg(p.slots + static_cast<int64_t>(r) * p.slot_cols + t);
+      d.target[t] = tg;
+      if (tg >= p.num_slots) flags |= KDA_DEVERR_SLOT;
+    }
+  }
+  d.status = flags ? kError : kLive;
+  return flags;
+}
+
+template <int T>
+__device__ __forceinline__ uint32_t small_bytes(const Params &p) {
+  return 3u * 256u * p.conv_width + 3u * T * 256u + 2u * T * 256u;
+}
+
+template <int T>
+__device__ __forceinline__ void issue_page(const Params &p, uint8_t *stage, int n,
+                                           const ItemDesc &d, uint64_t *bar,
+                                           uint64_t pol) {
+  const int h = n / p.batch;
+  const float *src = p.state + (static_cast<int64_t>(d.slot) * p.heads + h) *
+                                   static_cast<int64_t>(kDk * kDk);
+  bulk_g2s_hint(stage, src, kPageBytes, bar, pol);
+}
+
+template <int T>
+__device__ __forceinline__ void issue_small(const Params &p, uint8_t *stage, int n,
+                                            const ItemDesc &d, uint64_t *bar) {
+  const int h = n / p.batch;
+  const int r = n - h * p.batch;
+  const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
+  const uint32_t row_bytes = 256u * p.conv_width;  // 128 channels x W bf16
+#pragma unroll
+  for (int part = 0; part < 3; ++part) {
+    const __nv_bfloat16 *src =
+        p.conv_state + (static_cast<int64_t>(d.conv_slot) * 3 * dim + part * dim +
+                        static_cast<int64_t>(h) * kDk) *
+                           p.conv_width;
+    bulk_g2s(stage + p.conv_off + part * row_bytes, src, row_bytes, bar);
+  }
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    const int64_t row = static_cast<int64_t>(r) * T + t;
+#pragma unroll
+    for (int part = 0; part < 3; ++part)
+      bulk_g2s(stage + p.x_off + (t * 3 + part) * 256,
+               p.x + row * 3 * dim + part * dim + static_cast<int64_t>(h) * kDk, 256,
+               bar);
+    bulk_g2s(stage + p.gate_off + t * 256,
+             p.gate + row * dim + static_cast<int64_t>(h) * kDk, 256, bar);
+  }
+  bulk_g2s(stage + p.fa_off, p.f_a + static_cast<int64_t>(r) * T * kDk, T * 256u, bar);
+}
+
+template <int T, bool RECORD>
+__device__ void producer(const Params &p, uint8_t *smem, uint64_t *full,
+                         uint64_t *empty, ItemDesc *desc, int n0, int n1) {
+  const int S = p.stages;
+  const int count = n1 - n0;
+  const uint64_t pol = policy_evict_first();
+  const int pro = count < S ? count : S;
+  int issued = 0;
+  bool abort = false;
+
+  // Prologue: the first pages go out before waiting on the preceding kernel
+  // (state pool, slots and accepted are not its outputs).
+  for (int k = 0; k < pro; ++k) {
+    ItemDesc &d = desc[k];
+    const int flags = resolve_item<T, RECORD>(p, n0 + k, d);
+    if (flags && p.err) atomicOr(p.err, flags);
+    if (d.status == kLive) {
+      mbar_expect_tx(&full[k], kPageBytes);
+      issue_page<T>(p, smem + static_cast<size_t>(k) * p.stage_bytes, n0 + k, d,
+                    &full[k], pol);
+    }
+  }
+  griddep_wait();
+  for (int k = 0; k < pro; ++k) {
+    ItemDesc &d = desc[k];
+    const int r = (n0 + k) % p.batch;
+    const int h = (n0 + k) / p.batch;
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+      d.beta_bits[t] = __ldg(reinterpret_cast<const uint16_t *>(p.beta) +
+                             (static_cast<int64_t>(r) * T + t) * p.heads + h);
+    if (d.status == kLive) {
+      mbar_arrive_expect_tx(&full[k], small_bytes<T>(p));
+      issue_small<T>(p, smem + static_cast<size_t>(k) * p.stage_bytes, n0 + k, d,
+                     &full[k]);
+    } else {
+      mbar_arrive(&full[k]);
+    }
+    ++issued;
+  }
+  for (int k = pro; k < count; ++k) {
+    const int stage = k % S;
+    const uint32_t round = static_cast<uint32_t>(k / S);
+    if (!mbar_wait_bounded(&empty[stage], (round - 1u) & 1u)) {
+      abort = true;
+      break;
+    }
+    ItemDesc &d = desc[stage];
+    const int flags = resolve_item<T, RECORD>(p, n0 + k, d);
+    if (flags && p.err) atomicOr(p.err, flags);
+    const int r = (n0 + k) % p.batch;
+    const int h = (n0 + k) / p.batch;
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+      d.beta_bits[t] = __ldg(reinterpret_cast<const uint16_t *>(p.beta) +
+                             (static_cast<int64_t>(r) * T + t) * p.heads + h);
+    uint8_t *st = smem + static_cast<size_t>(stage) * p.stage_bytes;
+    if (d.status == kLive) {
+      mbar_arrive_expect_tx(&full[stage], kPageBytes + small_bytes<T>(p));
+      issue_page<T>(p, st, n0 + k, d, &full[stage], pol);
+      issue_small<T>(p, st, n0 + k, d, &full[stage]);
+    } else {
+      mbar_arrive(&full[stage]);
+    }
+    ++issued;
+  }
+  griddep_launch_dependents();
+  if (abort) {
+    if (p.err) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
+    // Drain: every copy issued into a stage must land before the CTA exits.
+    for (int k = (issued > S ? issued - S : 0); k < issued; ++k)
+      (void)mbar_wait_bounded(&full[k % S], static_cast<uint32_t>(k / S) & 1u);
+  }
+}
+
+// ----------------------------------------------------------------- consumers
+
+struct HeadConst {
+  uint32_t wa[8][4];   // f_b A fragments: [k chunk][a0..a3]
+  float wt[2][4];      // conv taps for this thread's parts
+  float bias[2];
+  float dt[2];         // dt_bias of features 16w+g, 16w+g+8
+  float ea;            // exp(A_log[h])
+};
+
+__device__ __forceinline__ void load_head_const(const Params &p, int h, int tid,
+                                                HeadConst &hc) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
+  const int fA = h * kDk + 16 * warp + g;
+  const uint2 *fb = reinterpret_cast<const uint2 *>(p.f_b);
+#pragma unroll
+  for (int kc = 0; kc < 8; ++kc) {
+    // Rank columns 16kc + 4q + {0,1,2,3} play the fragment's k positions
+    // {2q, 2q+1, 2q+8, 2q+9}; f_a uses the same permutation (sum unchanged).
+    const uint2 lo = __ldg(fb + (static_cast<int64_t>(fA) * kDk + 16 * kc + 4 * q) / 4);
+    const uint2 hi =
+        __ldg(fb + (static_cast<int64_t>(fA + 8) * kDk + 16 * kc + 4 * q) / 4);
+    hc.wa[kc][0] = lo.x;
+    hc.wa[kc][2] = lo.y;
+    hc.wa[kc][1] = hi.x;
+    hc.wa[kc][3] = hi.y;
+  }
+  const int c = tid & 127, sec = tid >> 7;
+  const uint16_t *cw = reinterpret_cast<const uint16_t *>(p.conv_weight);
+  const uint16_t *cb = reinterpret_cast<const uint16_t *>(p.conv_bias);
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int part = sec == 0 ? s : 2;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      hc.wt[s][i] = bf16_bits_to_float(
+          __ldg(cw + (static_cast<int64_t>(part) * 4 + i) * dim + h * kDk + c));
+    hc.bias[s] = p.has_bias
+                     ? bf16_bits_to_float(__ldg(cb + part * dim + h * kDk + c))
+                     : 0.0f;
+  }
+  hc.dt[0] = __ldg(p.dt_bias + h * kDk + 16 * warp + g);
+  hc.dt[1] = __ldg(p.dt_bias + h * kDk + 16 * warp + g + 8);
+  hc.ea = exp_approx(__ldg(p.a_log + h));
+}
+
+template <int T, bool RECORD>
+__device__ void consumer(const Params &p, uint8_t *smem, uint64_t *full,
+                         uint64_t *empty, const ItemDesc *desc, int n0, int n1) {
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int S = p.stages;
+  const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
+
+  float *front = reinterpret_cast<float *>(smem + p.front_off);
+  float *sq = front;                    // [T][128] q (then q_hat)
+  float *sk = sq + T * kDk;             // [T][128] k (then k_hat)
+  float *sv = sk + T * kDk;             // [T][128] v
+  float *sdec = sv + T * kDk;           // [T][128] decay
+  float *so = sdec + T * kDk;           // [T][128] o (BF16 values)
+  float *sbeta = so + T * kDk;          // [8]
+  float *ssum = sbeta + 8;              // [T][2][4] q, k squares per warp
+  float *osum = ssum + T * 8;           // [T][4]
+
+  const int c = tid & 127, sec = tid >> 7;
+  const float nw = bf16_bits_to_float(
+      __ldg(reinterpret_cast<const uint16_t *>(p.norm_weight) + c));
+  HeadConst hc;
+  int cur_head = -1;
+
+  for (int k = 0; k < n1 - n0; ++k) {
+    const int stage = k % S;
+    const uint32_t round = static_cast<uint32_t>(k / S);
+    const bool ok = mbar_wait_bounded(&full[stage], round & 1u);
+    if (consumer_sync_or(!ok)) {
+      if (tid == 0 && p.err) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
+      return;
+    }
+    const int n = n0 + k;
+    const int h = n / p.batch;
+    const int r = n - h * p.batch;
+    const ItemDesc &dsc = desc[stage];
+    const int status = dsc.status;
+    if (status != kLive) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (tid < kDk) {
+#pragma unroll
+        for (int t = 0; t < T; ++t)
+          p.output[(static_cast<int64_t>(r) * T + t) * dim + h * kDk + tid] =
+              __float2bfloat16_rn(0.0f);
+      }
+      continue;
+    }
+    const int slot = dsc.slot, cs = dsc.conv_slot, off = dsc.offset;
+    int target[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) target[t] = (T == 1) ? slot : (RECORD ? 0 : dsc.target[t]);
+    if (tid < T) sbeta[tid] = sigmoid_approx(bf16_bits_to_float(dsc.beta_bits[tid]));
+    if (h != cur_head) {
+      load_head_const(p, h, tid, hc);
+      cur_head = h;
+    }
+    const uint8_t *st = smem + static_cast<size_t>(stage) * p.stage_bytes;
+    const uint16_t *conv_s = reinterpret_cast<const uint16_t *>(st + p.conv_off);
+    const uint16_t *x_s = reinterpret_cast<const uint16_t *>(st + p.x_off);
+    const uint16_t *gate_s = reinterpret_cast<const uint16_t *>(st + p.gate_off);
+    const uint16_t *fa_s = reinterpret_cast<const uint16_t *>(st + p.fa_off);
+    const int64_t item = static_cast<int64_t>(r) * p.heads + h;
+
+    // --- convolution + SiLU + BF16 (KdaWide.kernel, "The convolution (stock
+    // tap order) and SiLU"); threads 0-127: q and k of channel c, 128-255: v.
+    float gv[T];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      if (sec == 1 && s == 1) break;
+      const int part = sec == 0 ? s : 2;
+      const uint16_t *row = conv_s + (part * kDk + c) * p.conv_width;
+      const uint16_t tap0 = row[off], tap1 = row[off + 1], tap2 = row[off + 2];
+      float win[3 + T];
+      win[0] = bf16_bits_to_float(tap0);
+      win[1] = bf16_bits_to_float(tap1);
+      win[2] = bf16_bits_to_float(tap2);
+      uint16_t xb[T];
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        xb[t] = x_s[(t * 3 + part) * kDk + c];
+        win[3 + t] = bf16_bits_to_float(xb[t]);
+      }
+      // New window [tap1, tap2, x_0 .. x_{T-1}] of this channel.
+      uint16_t *crow = reinterpret_cast<uint16_t *>(p.conv_state) +
+                       (static_cast<int64_t>(cs) * 3 * dim + part * dim + h * kDk + c) *
+                           p.conv_width;
+      crow[0] = tap1;
+      crow[1] = tap2;
+#pragma unroll
+      for (int t = 0; t < T; ++t) crow[2 + t] = xb[t];
+      float *dst = part == 0 ? sq : (part == 1 ? sk : sv);
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        float acc = hc.bias[s];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc = __fmaf_rn(win[t + i], hc.wt[s][i], acc);
+        const float y = bf16_round(silu_approx(acc));
+        dst[t * kDk + c] = y;
+        if (p.dbg)
+          p.dbg[((item * T + t) * 4 + part) * kDk + c] = __float2bfloat16_rn(y);
+        if (RECORD && part == 1)
+          p.rec_kg[(item * T + t) * 2 * kDk + c] = __float2bfloat16_rn(y);
+      }
+      if (sec == 0) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          const float y = dst[t * kDk + c];
+          const float sqsum = warp_sum(__fmul_rn(y, y));
+          if (lane == 0) ssum[(t * 2 + s) * 4 + warp] = sqsum;
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < T; ++t) gv[t] = bf16_bits_to_float(gate_s[t * kDk + c]);
+
+    // --- gate projection on tensor cores (KdaWide.kernel, "Gate projection"):
+    // D[feature, token] over 8 rank chunks of 16; token column n = lane/4.
+    {
+      const int g = lane >> 2, q = lane & 3;
+      uint32_t fb0[8], fb1[8];
+      const int ntok = g;
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc) {
+        if (ntok < T) {
+          const uint2 v =
+              *reinterpret_cast<const uint2 *>(fa_s + ntok * kDk + 16 * kc + 4 * q);
+          fb0[kc] = v.x;
+          fb1[kc] = v.y;
+        } else {
+          fb0[kc] = 0u;
+          fb1[kc] = 0u;
+        }
+      }
+      float acc[4][4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[m][e] = 0.0f;
+      if (p.gate_mode == 0) {
+#pragma unroll
+        for (int kc = 0; kc < 8; ++kc) mma_bf16(acc[0], hc.wa[kc], fb0[kc], fb1[kc]);
+      } else {
+#pragma unroll
+        for (int kc = 0; kc < 8; ++kc)
+          mma_bf16(acc[kc >> 1], hc.wa[kc], fb0[kc], fb1[kc]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = 2 * q + (e & 1);
+        const int f = 16 * warp + g + 8 * (e >> 1);
+        float value = acc[0][e];
+        if (p.gate_mode == 1)
+          value = __fadd_rn(
+              0.0f, __fadd_rn(__fadd_rn(__fadd_rn(value, acc[1][e]), acc[2][e]),
+                              acc[3][e]));
+        if (t < T) {
+          const __nv_bfloat16 gb = __float2bfloat16_rn(value);
+          const float raw = __bfloat162float(gb);
+          // KdaWide.decay
+          const float z = __fmul_rn(hc.ea, __fadd_rn(raw, hc.dt[e >> 1]));
+          const float dec = exp_approx(__fmul_rn(p.lower_bound, sigmoid_approx(z)));
+          sdec[t * kDk + f] = dec;
+          if (p.dbg) p.dbg[((item * T + t) * 4 + 3) * kDk + f] = gb;
+          if (RECORD) p.rec_kg[(item * T + t) * 2 * kDk + kDk + f] = gb;
+        }
+      }
+    }
+    consumer_sync();
+
+    // --- L2 norms ("Normalized q (with the 1/sqrt(K) scale) and k"),
+    // partial sums combined as KdaWide.quad_sum does.
+    if (sec == 0) {
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        const float *sq4 = ssum + t * 8;
+        const float qn = __fadd_rn(
+            __fadd_rn(__fadd_rn(sq4[0], sq4[2]), __fadd_rn(sq4[1], sq4[3])), 1.0e-6f);
+        const float kn = __fadd_rn(
+            __fadd_rn(__fadd_rn(sq4[4], sq4[6]), __fadd_rn(sq4[5], sq4[7])), 1.0e-6f);
+        const float fq = rcp_approx(sqrt_approx(qn));
+        const float fk = rcp_approx(sqrt_approx(kn));
+        sq[t * kDk + c] = __fmul_rn(__fmul_rn(sq[t * kDk + c], fq), p.scale);
+        sk[t * kDk + c] = __fmul_rn(sk[t * kDk + c], fk);
+      }
+    }
+    consumer_sync();
+
+    // --- recurrence ("The recurrence").  Page rows g + 32m, keys 32c + 4l + e.
+    const int g8 = tid >> 3, l8 = tid & 7;
+    const float *page_s = reinterpret_cast<const float *>(st);
+    float4 S[4][4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        S[m][cc] = *reinterpret_cast<const float4 *>(page_s + (g8 + 32 * m) * kDk +
+                                                     32 * cc + 4 * l8);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);  // stage free for the producer
+
+    const int mrow = (l8 >> 1) & 3;
+    const int my_row = g8 + 32 * mrow;
+#pragma unroll 1
+    for (int t = 0; t < T; ++t) {
+      float4 d4[4], k4[4], q4[4];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int key = 32 * cc + 4 * l8;
+        d4[cc] = *reinterpret_cast<const float4 *>(sdec + t * kDk + key);
+        k4[cc] = *reinterpret_cast<const float4 *>(sk + t * kDk + key);
+        q4[cc] = *reinterpret_cast<const float4 *>(sq + t * kDk + key);
+      }
+      float part[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float2 lo = __fmul2_rn(make_float2(S[m][cc].x, S[m][cc].y),
+                                 make_float2(d4[cc].x, d4[cc].y));
+          float2 hi = __fmul2_rn(make_float2(S[m][cc].z, S[m][cc].w),
+                                 make_float2(d4[cc].z, d4[cc].w));
+          S[m][cc] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          a0 = __ffma2_rn(lo, make_float2(k4[cc].x, k4[cc].y), a0);
+          a1 = __ffma2_rn(hi, make_float2(k4[cc].z, k4[cc].w), a1);
+        }
+        const float2 a = __fadd2_rn(a0, a1);
+        part[m] = __fadd_rn(a.x, a.y);
+      }
+      const float dot = reduce_scatter8(part, l8);
+      const float u = __fmul_rn(__fsub_rn(sv[t * kDk + my_row], dot), sbeta[t]);
+      if (RECORD && (l8 & 1) == 0)
+        p.rec_u[(item * T + t) * kDk + my_row] = u;
+      float U[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        U[m] = __shfl_sync(0xffffffffu, u, (lane & ~7) | (2 * m));
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
+        const float2 uu = make_float2(U[m], U[m]);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float2 lo = __ffma2_rn(make_float2(k4[cc].x, k4[cc].y), uu,
+                                 make_float2(S[m][cc].x, S[m][cc].y));
+          float2 hi = __ffma2_rn(make_float2(k4[cc].z, k4[cc].w), uu,
+                                 make_float2(S[m][cc].z, S[m][cc].w));
+          S[m][cc] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          a0 = __ffma2_rn(lo, make_float2(q4[cc].x, q4[cc].y), a0);
+          a1 = __ffma2_rn(hi, make_float2(q4[cc].z, q4[cc].w), a1);
+        }
+        const float2 a = __fadd2_rn(a0, a1);
+        part[m] = __fadd_rn(a.x, a.y);
+      }
+      const float o = reduce_scatter8(part, l8);
+      if ((l8 & 1) == 0) so[t * kDk + my_row] = bf16_round(o);
+      if (!RECORD) {
+        const int tgt = target[t];
+        if (tgt > 0) {
+          float *dstp = p.state + (static_cast<int64_t>(tgt) * p.heads + h) *
+                                      static_cast<int64_t>(kDk * kDk);
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+              __stcs(reinterpret_cast<float4 *>(dstp + (g8 + 32 * m) * kDk + 32 * cc +
+                                                4 * l8),
+                     S[m][cc]);
+        }
+      }
+    }
+    consumer_sync();
+
+    // --- gated RMSNorm epilogue ("Gated RMSNorm"), threads 0-127: channel c.
+    float ov[T];
+    if (sec == 0) {
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        ov[t] = so[t * kDk + c];
+        const float tot = warp_sum(__fmul_rn(ov[t], ov[t]));
+        if (lane == 0) osum[t * 4 + warp] = tot;
+      }
+    }
+    consumer_sync();
+    if (sec == 0) {
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        const float *o4 = osum + t * 4;
+        const float sumsq =
+            __fadd_rn(__fadd_rn(o4[0], o4[2]), __fadd_rn(o4[1], o4[3]));
+        const float var = __fadd_rn(__fmul_rn(sumsq, 1.0f / 128.0f), p.eps);
+        const float rstd = rcp_approx(sqrt_approx(var));
+        const float y = __fmul_rn(__fmul_rn(__fmul_rn(ov[t], rstd), nw),
+                                  sigmoid_approx(gv[t]));
+        p.output[(static_cast<int64_t>(r) * T + t) * dim + h * kDk + c] =
+            __float2bfloat16_rn(y);
+      }
+    }
+  }
+}
+
+template <int T, bool RECORD>
+__global__ void __launch_bounds__(kThreads, 1) kda_step_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);
+  uint64_t *empty = full + kMaxStages;
+  ItemDesc *desc = reinterpret_cast<ItemDesc *>(smem + p.desc_off);
+  const int G = gridDim.x;
+  const int n0 = static_cast<int>((static_cast<int64_t>(p.items) * blockIdx.x) / G);
+  const int n1 = static_cast<int>((static_cast<int64_t>(p.items) * (blockIdx.x + 1)) / G);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers / 32);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x >= kConsumers) {
+    if (threadIdx.x == kConsumers)
+      producer<T, RECORD>(p, smem, full, empty, desc, n0, n1);
+    return;
+  }
+  consumer<T, RECORD>(p, smem, full, empty, desc, n0, n1);
+}
+
+// ------------------------------------------------------------------ host side
+
+struct Layout {
+  uint32_t stage_bytes, conv_off, x_off, gate_off, fa_off;
+  uint32_t bar_off, desc_off, front_off, total;
+  int stages;
+};
+
+static uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+static bool make_layout(int T, int W, int max_smem, Layout &L) {
+  L.conv_off = kPageBytes;
+  L.x_off = align_up(L.conv_off + 3u * 256u * W, 128);
+  L.gate_off = L.x_off + 3u * T * 256u;
+  L.fa_off = L.gate_off + T * 256u;
+  L.stage_bytes = align_up(L.fa_off + T * 256u, 128);
+  const uint32_t tail = 2 * kMaxStages * 8 + kMaxStages * sizeof(ItemDesc) +
+                        (5u * T * kDk + 8 + T * 8 + T * 4) * 4;
+  for (int s = kMaxStages; s >= 2; --s) {
+    const uint32_t total = s * L.stage_bytes + tail;
+    if (total <= static_cast<uint32_t>(max_smem)) {
+      L.stages = s;
+      L.bar_off = s * L.stage_bytes;
+      L.desc_off = L.bar_off + 2 * kMaxStages * 8;
+      L.front_off = L.desc_off + kMaxStages * sizeof(ItemDesc);
+      L.total = total;
+      return true;
+    }
+  }
+  return false;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int max_smem = 0;
+  bool ok = false;
+  bool configured[KDA_MAX_TOKENS + 1][2] = {};
+};
+
+static DeviceInfo g_dev[64];
+
+template <int T, bool RECORD>
+static int launch_t(const Params &prm, const Layout &L, DeviceInfo &di, int grid,
+                    int use_pdl, cudaStream_t stream) {
+  auto kern = kda_step_kernel<T, RECORD>;
+  if (!di.configured[T][RECORD]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             di.max_smem) != cudaSuccess)
+      return KDA_ERR_LAUNCH;
+    di.configured[T][RECORD] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (use_pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) return KDA_ERR_LAUNCH;
+  return cudaGetLastError() == cudaSuccess ? KDA_SUCCESS : KDA_ERR_LAUNCH;
+}
+
+static bool aligned(const void *p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
+  if (!a) return KDA_ERR_NULL_ARGS;
+  const int T = a->tokens;
+  if (T < 1 || T > KDA_MAX_TOKENS) return KDA_ERR_TOKENS;
+  if (verify ? T == 1 : T != 1) return KDA_ERR_TOKENS;
+  if (a->gate_mode != 0 && a->gate_mode != 1) return KDA_ERR_GATE_MODE;
+  if (a->record && T == 1) return KDA_ERR_RECORD;
+  if (a->batch < 0 || a->heads < 0) return KDA_ERR_SHAPE;
+  if (a->batch == 0 || a->heads == 0) return KDA_SUCCESS;
+  if (a->num_slots < 1) return KDA_ERR_SHAPE;
+  if (T > 1 && a->slot_cols < T) return KDA_ERR_SHAPE;
+  if (static_cast<int64_t>(a->batch) * a->heads > 0x7fffffffLL) return KDA_ERR_SHAPE;
+  if (static_cast<int64_t>(a->heads) * kDk * 3 > 0x7fffffffLL) return KDA_ERR_SHAPE;
+  if (a->conv_width < T + 2) return KDA_ERR_CONV_WIDTH;
+  if (!a->x || !a->conv_weight || !a->f_a || !a->f_b || !a->beta || !a->gate ||
+      !a->norm_weight || !a->a_log || !a->dt_bias || !a->slots || !a->conv_state ||
+      !a->state || !a->output)
+    return KDA_ERR_NULL_POINTER;
+  if (a->has_bias && !a->conv_bias) return KDA_ERR_NULL_POINTER;
+  if (T > 1 && !a->accepted) return KDA_ERR_NULL_POINTER;
+  if (a->record && (!a->rec_u || !a->rec_kg)) return KDA_ERR_NULL_POINTER;
+  if (!aligned(a->state, 16) || !aligned(a->f_a, 16) || !aligned(a->f_b, 16) ||
+      !aligned(a->x, 16) || !aligned(a->gate, 16) || !aligned(a->conv_state, 16) ||
+      !aligned(a->conv_weight, 2) || !aligned(a->beta, 2) ||
+      !aligned(a->norm_weight, 2) || !aligned(a->output, 2) ||
+      !aligned(a->a_log, 4) || !aligned(a->dt_bias, 4) || !aligned(a->slots, 4) ||
+      (a->accepted && !aligned(a->accepted, 4)) ||
+      (a->has_bias && !aligned(a->conv_bias, 2)) ||
+      (a->rec_u && !aligned(a->rec_u, 4)) || (a->rec_kg && !aligned(a->rec_kg, 2)) ||
+      (a->err && !aligned(a->err, 4)) || (a->dbg && !aligned(a->dbg, 2)))
+    return KDA_ERR_ALIGNMENT;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KDA_ERR_DEVICE;
+  DeviceInfo &di = g_dev[dev];
+  if (!di.ok) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&di.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                               dev) != cudaSuccess)
+      return KDA_ERR_DEVICE;
+    if (major != 10 || minor != 3) return KDA_ERR_DEVICE;
+    di.ok = true;
+  }
+  Layout L;
+  if (!make_layout(T, a->conv_width, di.max_smem, L)) return KDA_ERR_CONV_WIDTH;
+
+  Params prm;
+  prm.batch = a->batch;
+  prm.heads = a->heads;
+  prm.num_slots = a->num_slots;
+  prm.conv_width = a->conv_width;
+  prm.slot_cols = T > 1 ? a->slot_cols : 1;
+  prm.gate_mode = a->gate_mode;
+  prm.has_bias = a->has_bias ? 1 : 0;
+  prm.items = a->batch * a->heads;
+  prm.stages = L.stages;
+  prm.stage_bytes = L.stage_bytes;
+  prm.conv_off = L.conv_off;
+  prm.x_off = L.x_off;
+  prm.gate_off = L.gate_off;
+  prm.fa_off = L.fa_off;
+  prm.bar_off = L.bar_off;
+  prm.desc_off = L.desc_off;
+  prm.front_off = L.front_off;
+  prm.x = static_cast<const __nv_bfloat16 *>(a->x);
+  prm.conv_weight = static_cast<const __nv_bfloat16 *>(a->conv_weight);
+  prm.conv_bias = static_cast<const __nv_bfloat16 *>(a->has_bias ? a->conv_bias : a->conv_weight);
+  prm.f_a = static_cast<const __nv_bfloat16 *>(a->f_a);
+  prm.f_b = static_cast<const __nv_bfloat16 *>(a->f_b);
+  prm.beta = static_cast<const __nv_bfloat16 *>(a->beta);
+  prm.gate = static_cast<const __nv_bfloat16 *>(a->gate);
+  prm.norm_weight = static_cast<const __nv_bfloat16 *>(a->norm_weight);
+  prm.a_log = a->a_log;
+  prm.dt_bias = a->dt_bias;
+  prm.slots = a->slots;
+  prm.accepted = a->accepted;
+  prm.conv_state = static_cast<__nv_bfloat16 *>(a->conv_state);
+  prm.state = a->state;
+  prm.output = static_cast<__nv_bfloat16 *>(a->output);
+  prm.rec_u = a->rec_u;
+  prm.rec_kg = static_cast<__nv_bfloat16 *>(a->rec_kg);
+  prm.lower_bound = a->lower_bound;
+  prm.scale = a->scale;
+  prm.eps = a->eps;
+  prm.err = a->err;
+  prm.dbg = static_cast<__nv_bfloat16 *>(a->dbg);
+
+  const int grid = prm.items < di.sms ? prm.items : di.sms;
+  const int pdl = a->use_pdl ? 1 : 0;
+  const bool rec = a->record != 0;
+  switch (T) {
+    case 1: return launch_t<1, false>(prm, L, di, grid, pdl, stream);
+    case 2: return rec ? launch_t<2, true>(prm, L, di, grid, pdl, stream)
+                       : launch_t<2, false>(prm, L, di, grid, pdl, stream);
+    case 3: return rec ? launch_t<3, true>(prm, L, di, grid, pdl, stream)
+                       : launch_t<3, false>(prm, L, di, grid, pdl, stream);
+    case 4: return rec ? launch_t<4, true>(prm, L, di, grid, pdl, stream)
+                       : launch_t<4, false>(prm, L, di, grid, pdl, stream);
+    case 5: return rec ? launch_t<5, true>(prm, L, di, grid, pdl, stream)
+                       : launch_t<5, false>(prm, L, di, grid, pdl, stream);
+    case 6: return rec ? launch_t<6, true>(prm, L, di, grid, pdl, stream)
+                       : launch_t<6, false>(prm, L, di, grid, pdl, stream);
+    case 7: return rec ? launch_t<7, true>(prm, L, di, grid, pdl, stream)
+                       : launch_t<7, false>(prm, L, di, grid, pdl, stream);
+    default: return rec ? launch_t<8, true>(prm, L, di, grid, pdl, stream)
+                        : launch_t<8, false>(prm, L, di, grid, pdl, stream);
+  }
+}
+
+}  // namespace kda
+
+extern "C" {
+
+int kda_decode(const kda_args *args, void *stream) {
+  return kda::run_step(args, static_cast<cudaStream_t>(stream), false);
+}
+
+int kda_verify(const kda_args *args, void *stream) {
+  return kda::run_step(args, static_cast<cudaStream_t>(stream), true);
+}
+
+const char *kda_strerror(int code) {
+  switch (code) {
+    case KDA_SUCCESS: return "success";
+    case KDA_ERR_NULL_ARGS: return "args is NULL";
+    case KDA_ERR_TOKENS: return "tokens outside 1..8 or wrong entry point for tokens";
+    case KDA_ERR_GATE_MODE: return "gate_mode must be 0 or 1";
+    case KDA_ERR_RECORD: return "record mode needs tokens > 1";
+    case KDA_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case KDA_ERR_CONV_WIDTH: return "conv_width < tokens + 2, or too wide to stage";
+    case KDA_ERR_ALIGNMENT: return "a pointer is not aligned as required";
+    case KDA_ERR_SHAPE: return "invalid sizes";
+    case KDA_ERR_DEVICE: return "no usable sm_103 device";
+    case KDA_ERR_LAUNCH: return "kernel launch failed";
+    default: return "unknown error code";
+  }
+}
+
+int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+}  // extern "C"

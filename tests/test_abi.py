@@ -1,0 +1,83 @@
+"""The C-ABI library builds, loads and exports every function include/kda.h
+declares; host-side argument validation answers without touching a GPU."""
+from __future__ import annotations
+
+import os
+import re
+
+import pytest
+
+from linear_attention_recurrent_kda_gb300 import build as kbuild
+from linear_attention_recurrent_kda_gb300 import lib as kl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(kda_\w+)\s*\(",
+                                text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    kbuild.build()
+    lib = kl.load()
+    names = declared_functions()
+    assert set(kl.EXPORTED) <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_version_and_strerror():
+    assert kl.load().kda_abi_version() == 1
+    for code in range(0, 11):
+        assert kl.strerror(code)
+    assert "unknown" in kl.strerror(999)
+
+
+def _args(**kw):
+    a = kl.KdaArgs()
+    a.batch, a.heads, a.tokens, a.num_slots, a.conv_width = 2, 1, 1, 4, 3
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_null_args():
+    import ctypes
+    lib = kl.load()
+    assert lib.kda_decode(None, None) == kl.KDA_ERR_NULL_ARGS
+    assert lib.kda_verify(None, None) == kl.KDA_ERR_NULL_ARGS
+
+
+@pytest.mark.parametrize("entry,kw,code", [
+    ("kda_decode", dict(tokens=0), kl.KDA_ERR_TOKENS),
+    ("kda_decode", dict(tokens=2), kl.KDA_ERR_TOKENS),
+    ("kda_verify", dict(tokens=1), kl.KDA_ERR_TOKENS),
+    ("kda_verify", dict(tokens=9), kl.KDA_ERR_TOKENS),
+    ("kda_decode", dict(gate_mode=3), kl.KDA_ERR_GATE_MODE),
+    ("kda_decode", dict(record=1), kl.KDA_ERR_RECORD),
+    ("kda_decode", dict(batch=-1), kl.KDA_ERR_SHAPE),
+    ("kda_decode", dict(batch=0), kl.KDA_SUCCESS),
+    ("kda_decode", dict(heads=0), kl.KDA_SUCCESS),
+    ("kda_decode", dict(num_slots=0), kl.KDA_ERR_SHAPE),
+    ("kda_verify", dict(tokens=3, slot_cols=2, conv_width=5), kl.KDA_ERR_SHAPE),
+    ("kda_decode", dict(conv_width=2), kl.KDA_ERR_CONV_WIDTH),
+    ("kda_decode", {}, kl.KDA_ERR_NULL_POINTER),
+])
+def test_host_validation_without_gpu(entry, kw, code):
+    assert kl.call(entry, _args(**kw), 0) == code
+
+
+def test_alignment_rule_checked_before_any_device_call():
+    a = _args()
+    fake = 1 << 20
+    for name in ("x", "conv_weight", "f_a", "f_b", "beta", "gate", "norm_weight",
+                 "a_log", "dt_bias", "slots", "conv_state", "state", "output"):
+        setattr(a, name, fake)
+    a.state = fake + 4            # FP32 pool must be 16-byte aligned
+    assert kl.call("kda_decode", a, 0) == kl.KDA_ERR_ALIGNMENT
