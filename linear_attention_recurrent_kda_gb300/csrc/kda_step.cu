@@ -6,24 +6,33 @@
 // step it runs are described in include/kda.h.
 //
 // Design (GB300-first; the page's one-CTA-per-item kernel is prior art):
-//   * Persistent kernel, one CTA per SM.  Each CTA owns a contiguous range of
-//     items in head-major order (item = h * batch + r), so the per-head
-//     constants (f_b tensor-core fragments, conv weights, dt_bias) stay in
-//     registers across its items.
-//   * Warp 8 is the producer: per item it resolves the slots, loads the
-//     scalar inputs (beta, targets) into an item descriptor and stages the
-//     64 KiB FP32 state page plus the item's conv rows, x, gate and f_a rows
-//     into a shared-memory ring of 2-3 stages with cp.async.bulk (TMA bulk
-//     copies) signalling an mbarrier.  It runs 2-3 items ahead, so the HBM
-//     read of later pages overlaps the compute of the current one.
-//   * Warps 0-7 are consumers.  Front: conv + SiLU (threads own channels),
-//     gate projection on tensor cores (mma.sync m16n8k16 BF16, FP32 accumulate,
-//     warp w owns features 16w..16w+15), decay, beta, L2 norms.  Recurrence:
-//     thread (g = tid/8, l = tid%8) holds keys {32c + 4l + e} of value rows
-//     g, g+32, g+64, g+96 in registers (64 floats), packed FP32 FMAs
-//     (f32x2), row reductions as an 8-lane reduce-scatter.  The updated page
-//     goes straight from registers to HBM with 16-byte streaming stores.
-//   * Every wait is bounded (wall clock) and reports KDA_DEVERR_TIMEOUT.
+//   * Persistent kernel, one CTA of four warpgroups per SM.  Each CTA owns a
+//     contiguous range of items in head-major order (item = h * batch + r), so
+//     the per-head f_b tensor-core fragments stay in registers across its
+//     items.
+//   * Three warp roles work on consecutive items at the same time:
+//       producer   (warpgroup 3, one thread): per item resolves the slots,
+//                  loads beta and the write targets into an item descriptor and
+//                  stages the 64 KiB FP32 state page plus the item's conv rows,
+//                  x, gate and f_a rows into a 2-3 stage shared-memory ring
+//                  with TMA bulk copies completing on an mbarrier; it runs 2-3
+//                  items ahead;
+//       front      (warpgroup 2): item j's conv + SiLU, gate projection on
+//                  tensor cores (mma.sync m16n8k16 BF16, FP32 accumulate),
+//                  decay, beta, L2 norms, sigmoid(gate) -> a double-buffered
+//                  hand-off slot;
+//       recurrence (warpgroups 0-1): item j-1's delta rule with the page in
+//                  registers: thread (g = tid/8, l = tid%8) holds keys
+//                  {32c + 4l + e} of value rows g, g+32, g+64, g+96 (64
+//                  floats), packed FP32 (f32x2) multiplies/FMAs, row sums by an
+//                  8-lane reduce-scatter; the page goes from registers to HBM
+//                  with 16-byte streaming stores after every token; then the
+//                  gated RMSNorm epilogue of the item.
+//     The time per item is max(front, recurrence), not their sum.
+//   * setmaxnreg moves registers from the producer warpgroup (40 a thread) to
+//     the recurrence (160) and front (144) warpgroups; launch gives 128.
+//   * Every wait is bounded (wall clock); a timeout raises a shared abort flag
+//     that stops every role, and KDA_DEVERR_TIMEOUT is reported.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -32,13 +41,23 @@
 
 namespace kda {
 
-constexpr int kDk = 128;                    // dk = dv = gate rank
-constexpr int kConsumers = 256;             // warps 0-7
-constexpr int kThreads = kConsumers + 32;   // + producer warp 8
+constexpr int kDk = 128;                          // dk = dv = gate rank
+constexpr int kRecThreads = 256;                  // warpgroups 0-1
+constexpr int kFrontThreads = 128;                // warpgroup 2
+constexpr int kProducer = kRecThreads + kFrontThreads;  // warpgroup 3, thread 0
+constexpr int kThreads = kProducer + 128;
+constexpr int kRecRegs = 160;                     // setmaxnreg split (launch: 128)
+constexpr int kFrontRegs = 144;
+constexpr int kProducerRegs = 40;
 constexpr uint32_t kPageBytes = kDk * kDk * 4;
 constexpr int kMaxStages = 3;
+constexpr int kSlots = 2;                         // front -> recurrence hand-off
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kLive = 0, kPad = 1, kError = 2;
+
+static_assert(kRecThreads * kRecRegs + kFrontThreads * kFrontRegs + 128 * kProducerRegs <=
+                  kThreads * 128,
+              "register split exceeds the launch allocation");
 
 struct __align__(16) ItemDesc {
   int32_t status;
@@ -53,7 +72,7 @@ struct Params {
   int32_t batch, heads, num_slots, conv_width, slot_cols, gate_mode, has_bias;
   int32_t items, stages;
   uint32_t stage_bytes, conv_off, x_off, gate_off, fa_off;
-  uint32_t bar_off, desc_off, front_off;
+  uint32_t bar_off, desc_off, slot_off, slot_bytes, scratch_off, rscratch_off;
   const __nv_bfloat16 *x, *conv_weight, *conv_bias, *f_a, *f_b, *beta, *gate,
       *norm_weight;
   const float *a_log, *dt_bias;
@@ -66,6 +85,15 @@ struct Params {
   float lower_bound, scale, eps;
   int32_t *err;
   __nv_bfloat16 *dbg;
+};
+
+// Shared-memory control block (barriers, abort flag), at p.bar_off.
+struct Ctrl {
+  uint64_t full[kMaxStages];   // producer -> front + recurrence (bytes landed)
+  uint64_t empty[kMaxStages];  // front + recurrence -> producer (stage free)
+  uint64_t fready[kSlots];     // front -> recurrence (slot inputs written)
+  uint64_t sfree[kSlots];      // recurrence -> front (slot consumed)
+  uint32_t abort;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -119,15 +147,35 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Waits for the phase of `parity` to complete; false after kWaitLimitNs of
-// wall clock (or 2^30 polls, whichever first).
-__device__ __noinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `hint_ns` pass, instead of spinning on issue slots that
+// the other roles' warps on the same SM sub-partition need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `parity` to complete.  Returns false, and raises the
+// CTA's abort flag, after kWaitLimitNs of wall clock (or 2^24 sleeps); returns
+// false early when another thread raised the flag.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile uint32_t *abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  for (uint32_t it = 1; it < (1u << 30); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  for (uint32_t it = 0; it < (1u << 24); ++it) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) break;
   }
+  *abort_flag = 1u;
   return false;
 }
 
@@ -157,16 +205,34 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src,
       : "memory");
 }
 
-__device__ __forceinline__ void consumer_sync() {
+// Named barrier 1 over the 256 recurrence threads.
+__device__ __forceinline__ void rec_sync() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
-// Barrier over the 256 consumer threads that also ORs a predicate.
-__device__ __forceinline__ bool consumer_sync_or(bool pred) {
+// Named barrier 1 over the 256 recurrence threads that also ORs a predicate.
+__device__ __forceinline__ bool rec_sync_or(bool pred) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
       " bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
+
+// Named barrier 2 over the 128 front threads.
+__device__ __forceinline__ void front_sync() {
+  asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+
+// Named barrier 2 over the 128 front threads that also ORs a predicate.
+__device__ __forceinline__ bool front_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " bar.red.or.pred q, 2, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
       : "=r"(r)
       : "r"(static_cast<uint32_t>(pred))
       : "memory");
@@ -178,6 +244,15 @@ __device__ __forceinline__ void griddep_wait() {
 }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // m16n8k16 BF16 tensor-core MMA, FP32 accumulate in place.
@@ -253,6 +328,26 @@ __device__ __forceinline__ float reduce_scatter8(const float (&x)[4], int l) {
   return keep;
 }
 
+// Hand-off slot between the front and the recurrence (one per live item in
+// flight): FP32 [T][128] arrays and the item's scalars.
+template <int T>
+struct SlotView {
+  float *q, *k, *d, *v, *sg, *o, *beta;
+  int32_t *tgt, *meta;
+  __device__ __forceinline__ explicit SlotView(uint8_t *base) {
+    float *f = reinterpret_cast<float *>(base);
+    q = f;
+    k = q + T * kDk;
+    d = k + T * kDk;
+    v = d + T * kDk;
+    sg = v + T * kDk;
+    o = sg + T * kDk;
+    beta = o + T * kDk;
+    tgt = reinterpret_cast<int32_t *>(beta + KDA_MAX_TOKENS);
+    meta = tgt + KDA_MAX_TOKENS;
+  }
+};
+
 // ----------------------------------------------------------------- producer
 
 template <int T, bool RECORD>
@@ -301,7 +396,6 @@ __device__ __forceinline__ uint32_t small_bytes(const Params &p) {
   return 3u * 256u * p.conv_width + 3u * T * 256u + 2u * T * 256u;
 }
 
-template <int T>
 __device__ __forceinline__ void issue_page(const Params &p, uint8_t *stage, int n,
                                            const ItemDesc &d, uint64_t *bar,
                                            uint64_t pol) {
@@ -340,15 +434,25 @@ __device__ __forceinline__ void issue_small(const Params &p, uint8_t *stage, int
   bulk_g2s(stage + p.fa_off, p.f_a + static_cast<int64_t>(r) * T * kDk, T * 256u, bar);
 }
 
+template <int T>
+__device__ __forceinline__ void load_beta(const Params &p, int n, ItemDesc &d) {
+  const int h = n / p.batch;
+  const int r = n - h * p.batch;
+#pragma unroll
+  for (int t = 0; t < T; ++t)
+    d.beta_bits[t] = __ldg(reinterpret_cast<const uint16_t *>(p.beta) +
+                           (static_cast<int64_t>(r) * T + t) * p.heads + h);
+}
+
 template <int T, bool RECORD>
-__device__ void producer(const Params &p, uint8_t *smem, uint64_t *full,
-                         uint64_t *empty, ItemDesc *desc, int n0, int n1) {
+__device__ void producer_role(const Params &p, uint8_t *smem, Ctrl *ctl,
+                              ItemDesc *desc, int n0, int n1) {
   const int S = p.stages;
   const int count = n1 - n0;
   const uint64_t pol = policy_evict_first();
   const int pro = count < S ? count : S;
   int issued = 0;
-  bool abort = false;
+  bool aborted = false;
 
   // Prologue: the first pages go out before waiting on the preceding kernel
   // (state pool, slots and accepted are not its outputs).
@@ -357,371 +461,421 @@ __device__ void producer(const Params &p, uint8_t *smem, uint64_t *full,
     const int flags = resolve_item<T, RECORD>(p, n0 + k, d);
     if (flags && p.err) atomicOr(p.err, flags);
     if (d.status == kLive) {
-      mbar_expect_tx(&full[k], kPageBytes);
-      issue_page<T>(p, smem + static_cast<size_t>(k) * p.stage_bytes, n0 + k, d,
-                    &full[k], pol);
+      mbar_expect_tx(&ctl->full[k], kPageBytes);
+      issue_page(p, smem + static_cast<size_t>(k) * p.stage_bytes, n0 + k, d,
+                 &ctl->full[k], pol);
     }
   }
   griddep_wait();
   for (int k = 0; k < pro; ++k) {
     ItemDesc &d = desc[k];
-    const int r = (n0 + k) % p.batch;
-    const int h = (n0 + k) / p.batch;
-#pragma unroll
-    for (int t = 0; t < T; ++t)
-      d.beta_bits[t] = __ldg(reinterpret_cast<const uint16_t *>(p.beta) +
-                             (static_cast<int64_t>(r) * T + t) * p.heads + h);
+    load_beta<T>(p, n0 + k, d);
     if (d.status == kLive) {
-      mbar_arrive_expect_tx(&full[k], small_bytes<T>(p));
+      mbar_arrive_expect_tx(&ctl->full[k], small_bytes<T>(p));
       issue_small<T>(p, smem + static_cast<size_t>(k) * p.stage_bytes, n0 + k, d,
-                     &full[k]);
+                     &ctl->full[k]);
     } else {
-      mbar_arrive(&full[k]);
+      mbar_arrive(&ctl->full[k]);
     }
     ++issued;
   }
   for (int k = pro; k < count; ++k) {
     const int stage = k % S;
     const uint32_t round = static_cast<uint32_t>(k / S);
-    if (!mbar_wait_bounded(&empty[stage], (round - 1u) & 1u)) {
-      abort = true;
+    if (!mbar_wait(&ctl->empty[stage], (round - 1u) & 1u, &ctl->abort)) {
+      aborted = true;
       break;
     }
     ItemDesc &d = desc[stage];
     const int flags = resolve_item<T, RECORD>(p, n0 + k, d);
     if (flags && p.err) atomicOr(p.err, flags);
-    const int r = (n0 + k) % p.batch;
-    const int h = (n0 + k) / p.batch;
-#pragma unroll
-    for (int t = 0; t < T; ++t)
-      d.beta_bits[t] = __ldg(reinterpret_cast<const uint16_t *>(p.beta) +
-                             (static_cast<int64_t>(r) * T + t) * p.heads + h);
+    load_beta<T>(p, n0 + k, d);
     uint8_t *st = smem + static_cast<size_t>(stage) * p.stage_bytes;
     if (d.status == kLive) {
-      mbar_arrive_expect_tx(&full[stage], kPageBytes + small_bytes<T>(p));
-      issue_page<T>(p, st, n0 + k, d, &full[stage], pol);
-      issue_small<T>(p, st, n0 + k, d, &full[stage]);
+      mbar_arrive_expect_tx(&ctl->full[stage], kPageBytes + small_bytes<T>(p));
+      issue_page(p, st, n0 + k, d, &ctl->full[stage], pol);
+      issue_small<T>(p, st, n0 + k, d, &ctl->full[stage]);
     } else {
-      mbar_arrive(&full[stage]);
+      mbar_arrive(&ctl->full[stage]);
     }
     ++issued;
   }
   griddep_launch_dependents();
-  if (abort) {
+  if (aborted || ctl->abort) {
     if (p.err) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
     // Drain: every copy issued into a stage must land before the CTA exits.
+    uint32_t keep_waiting = 0;
     for (int k = (issued > S ? issued - S : 0); k < issued; ++k)
-      (void)mbar_wait_bounded(&full[k % S], static_cast<uint32_t>(k / S) & 1u);
+      (void)mbar_wait(&ctl->full[k % S], static_cast<uint32_t>(k / S) & 1u,
+                      &keep_waiting);
   }
 }
 
-// ----------------------------------------------------------------- consumers
+// ----------------------------------------------------------------- front
 
-struct HeadConst {
-  uint32_t wa[8][4];   // f_b A fragments: [k chunk][a0..a3]
-  float wt[2][4];      // conv taps for this thread's parts
-  float bias[2];
-  float dt[2];         // dt_bias of features 16w+g, 16w+g+8
-  float ea;            // exp(A_log[h])
+// Per-head constants kept in registers across a CTA's items of one head: the
+// f_b fragments of this warp's 32 features, the conv taps and bias of this
+// thread's channel, dt_bias of its MMA features and exp(A_log).
+struct FrontConst {
+  uint32_t wa[2][8][4];  // f_b A fragments: [tile][k chunk][a0..a3]
+  float wt[3][4];        // conv taps of channel c, parts q, k, v
+  float bias[3];
+  float dt[2][2];        // dt_bias of features 32w + 16m + g + 8i
+  float ea;              // exp(A_log[h])
 };
 
-__device__ __forceinline__ void load_head_const(const Params &p, int h, int tid,
-                                                HeadConst &hc) {
-  const int warp = tid >> 5, lane = tid & 31;
+__device__ __forceinline__ void load_front_const(const Params &p, int h, int c,
+                                                 FrontConst &fc) {
+  const int fw = c >> 5, lane = c & 31;
   const int g = lane >> 2, q = lane & 3;
   const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
-  const int fA = h * kDk + 16 * warp + g;
   const uint2 *fb = reinterpret_cast<const uint2 *>(p.f_b);
 #pragma unroll
-  for (int kc = 0; kc < 8; ++kc) {
-    // Rank columns 16kc + 4q + {0,1,2,3} play the fragment's k positions
-    // {2q, 2q+1, 2q+8, 2q+9}; f_a uses the same permutation (sum unchanged).
-    const uint2 lo = __ldg(fb + (static_cast<int64_t>(fA) * kDk + 16 * kc + 4 * q) / 4);
-    const uint2 hi =
-        __ldg(fb + (static_cast<int64_t>(fA + 8) * kDk + 16 * kc + 4 * q) / 4);
-    hc.wa[kc][0] = lo.x;
-    hc.wa[kc][2] = lo.y;
-    hc.wa[kc][1] = hi.x;
-    hc.wa[kc][3] = hi.y;
+  for (int m = 0; m < 2; ++m) {
+    const int fA = h * kDk + 32 * fw + 16 * m + g;
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc) {
+      // Rank columns 16kc + 4q + {0,1,2,3} play the fragment's k positions
+      // {2q, 2q+1, 2q+8, 2q+9}; f_a uses the same permutation (sum unchanged).
+      const uint2 lo =
+          __ldg(fb + (static_cast<int64_t>(fA) * kDk + 16 * kc + 4 * q) / 4);
+      const uint2 hi =
+          __ldg(fb + (static_cast<int64_t>(fA + 8) * kDk + 16 * kc + 4 * q) / 4);
+      fc.wa[m][kc][0] = lo.x;
+      fc.wa[m][kc][2] = lo.y;
+      fc.wa[m][kc][1] = hi.x;
+      fc.wa[m][kc][3] = hi.y;
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      fc.dt[m][i] = __ldg(p.dt_bias + h * kDk + 32 * fw + 16 * m + g + 8 * i);
   }
-  const int c = tid & 127, sec = tid >> 7;
   const uint16_t *cw = reinterpret_cast<const uint16_t *>(p.conv_weight);
   const uint16_t *cb = reinterpret_cast<const uint16_t *>(p.conv_bias);
 #pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    const int part = sec == 0 ? s : 2;
+  for (int part = 0; part < 3; ++part) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      hc.wt[s][i] = bf16_bits_to_float(
+      fc.wt[part][i] = bf16_bits_to_float(
           __ldg(cw + (static_cast<int64_t>(part) * 4 + i) * dim + h * kDk + c));
-    hc.bias[s] = p.has_bias
-                     ? bf16_bits_to_float(__ldg(cb + part * dim + h * kDk + c))
-                     : 0.0f;
+    fc.bias[part] = p.has_bias
+                        ? bf16_bits_to_float(__ldg(cb + part * dim + h * kDk + c))
+                        : 0.0f;
   }
-  hc.dt[0] = __ldg(p.dt_bias + h * kDk + 16 * warp + g);
-  hc.dt[1] = __ldg(p.dt_bias + h * kDk + 16 * warp + g + 8);
-  hc.ea = exp_approx(__ldg(p.a_log + h));
+  fc.ea = exp_approx(__ldg(p.a_log + h));
 }
 
+// Front of one live item: conv + SiLU + BF16, gate projection + decay, beta,
+// L2 norms, written to slot `sv`.  Releases the stage once its reads are done.
 template <int T, bool RECORD>
-__device__ void consumer(const Params &p, uint8_t *smem, uint64_t *full,
-                         uint64_t *empty, const ItemDesc *desc, int n0, int n1) {
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int S = p.stages;
+__device__ __forceinline__ void front_item(const Params &p, const uint8_t *st,
+                                           const ItemDesc &dsc, int n,
+                                           const SlotView<T> &sv, float *ssum,
+                                           const FrontConst &fc, int c,
+                                           uint64_t *empty_bar) {
+  const int fw = c >> 5, lane = c & 31;
+  const int h = n / p.batch;
+  const int r = n - h * p.batch;
   const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
+  const int64_t item = static_cast<int64_t>(r) * p.heads + h;
+  const int cs = dsc.conv_slot, off = dsc.offset;
+  const uint16_t *conv_s = reinterpret_cast<const uint16_t *>(st + p.conv_off);
+  const uint16_t *x_s = reinterpret_cast<const uint16_t *>(st + p.x_off);
+  const uint16_t *gate_s = reinterpret_cast<const uint16_t *>(st + p.gate_off);
+  const uint16_t *fa_s = reinterpret_cast<const uint16_t *>(st + p.fa_off);
 
-  float *front = reinterpret_cast<float *>(smem + p.front_off);
-  float *sq = front;                    // [T][128] q (then q_hat)
-  float *sk = sq + T * kDk;             // [T][128] k (then k_hat)
-  float *sv = sk + T * kDk;             // [T][128] v
-  float *sdec = sv + T * kDk;           // [T][128] decay
-  float *so = sdec + T * kDk;           // [T][128] o (BF16 values)
-  float *sbeta = so + T * kDk;          // [8]
-  float *ssum = sbeta + 8;              // [T][2][4] q, k squares per warp
-  float *osum = ssum + T * 8;           // [T][4]
-
-  const int c = tid & 127, sec = tid >> 7;
-  const float nw = bf16_bits_to_float(
-      __ldg(reinterpret_cast<const uint16_t *>(p.norm_weight) + c));
-  HeadConst hc;
-  int cur_head = -1;
-
-  for (int k = 0; k < n1 - n0; ++k) {
-    const int stage = k % S;
-    const uint32_t round = static_cast<uint32_t>(k / S);
-    const bool ok = mbar_wait_bounded(&full[stage], round & 1u);
-    if (consumer_sync_or(!ok)) {
-      if (tid == 0 && p.err) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
-      return;
+  // --- convolution + SiLU + BF16 (KdaWide.kernel, "The convolution (stock
+  // tap order) and SiLU"): this thread owns channel c of q, k and v.
+#pragma unroll
+  for (int part = 0; part < 3; ++part) {
+    const uint16_t *row = conv_s + (part * kDk + c) * p.conv_width;
+    const uint16_t tap0 = row[off], tap1 = row[off + 1], tap2 = row[off + 2];
+    float win[3 + T];
+    win[0] = bf16_bits_to_float(tap0);
+    win[1] = bf16_bits_to_float(tap1);
+    win[2] = bf16_bits_to_float(tap2);
+    uint16_t xb[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      xb[t] = x_s[(t * 3 + part) * kDk + c];
+      win[3 + t] = bf16_bits_to_float(xb[t]);
     }
-    const int n = n0 + k;
-    const int h = n / p.batch;
-    const int r = n - h * p.batch;
-    const ItemDesc &dsc = desc[stage];
-    const int status = dsc.status;
-    if (status != kLive) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      if (tid < kDk) {
+    // New window [tap1, tap2, x_0 .. x_{T-1}] of this channel.
+    uint16_t *crow = reinterpret_cast<uint16_t *>(p.conv_state) +
+                     (static_cast<int64_t>(cs) * 3 * dim + part * dim + h * kDk + c) *
+                         p.conv_width;
+    crow[0] = tap1;
+    crow[1] = tap2;
 #pragma unroll
-        for (int t = 0; t < T; ++t)
-          p.output[(static_cast<int64_t>(r) * T + t) * dim + h * kDk + tid] =
-              __float2bfloat16_rn(0.0f);
-      }
-      continue;
-    }
-    const int slot = dsc.slot, cs = dsc.conv_slot, off = dsc.offset;
-    int target[T];
+    for (int t = 0; t < T; ++t) crow[2 + t] = xb[t];
+    float *dst = part == 0 ? sv.q : (part == 1 ? sv.k : sv.v);
 #pragma unroll
-    for (int t = 0; t < T; ++t) target[t] = (T == 1) ? slot : (RECORD ? 0 : dsc.target[t]);
-    if (tid < T) sbeta[tid] = sigmoid_approx(bf16_bits_to_float(dsc.beta_bits[tid]));
-    if (h != cur_head) {
-      load_head_const(p, h, tid, hc);
-      cur_head = h;
-    }
-    const uint8_t *st = smem + static_cast<size_t>(stage) * p.stage_bytes;
-    const uint16_t *conv_s = reinterpret_cast<const uint16_t *>(st + p.conv_off);
-    const uint16_t *x_s = reinterpret_cast<const uint16_t *>(st + p.x_off);
-    const uint16_t *gate_s = reinterpret_cast<const uint16_t *>(st + p.gate_off);
-    const uint16_t *fa_s = reinterpret_cast<const uint16_t *>(st + p.fa_off);
-    const int64_t item = static_cast<int64_t>(r) * p.heads + h;
-
-    // --- convolution + SiLU + BF16 (KdaWide.kernel, "The convolution (stock
-    // tap order) and SiLU"); threads 0-127: q and k of channel c, 128-255: v.
-    float gv[T];
+    for (int t = 0; t < T; ++t) {
+      float acc = fc.bias[part];
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      if (sec == 1 && s == 1) break;
-      const int part = sec == 0 ? s : 2;
-      const uint16_t *row = conv_s + (part * kDk + c) * p.conv_width;
-      const uint16_t tap0 = row[off], tap1 = row[off + 1], tap2 = row[off + 2];
-      float win[3 + T];
-      win[0] = bf16_bits_to_float(tap0);
-      win[1] = bf16_bits_to_float(tap1);
-      win[2] = bf16_bits_to_float(tap2);
-      uint16_t xb[T];
-#pragma unroll
-      for (int t = 0; t < T; ++t) {
-        xb[t] = x_s[(t * 3 + part) * kDk + c];
-        win[3 + t] = bf16_bits_to_float(xb[t]);
-      }
-      // New window [tap1, tap2, x_0 .. x_{T-1}] of this channel.
-      uint16_t *crow = reinterpret_cast<uint16_t *>(p.conv_state) +
-                       (static_cast<int64_t>(cs) * 3 * dim + part * dim + h * kDk + c) *
-                           p.conv_width;
-      crow[0] = tap1;
-      crow[1] = tap2;
-#pragma unroll
-      for (int t = 0; t < T; ++t) crow[2 + t] = xb[t];
-      float *dst = part == 0 ? sq : (part == 1 ? sk : sv);
-#pragma unroll
-      for (int t = 0; t < T; ++t) {
-        float acc = hc.bias[s];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc = __fmaf_rn(win[t + i], hc.wt[s][i], acc);
-        const float y = bf16_round(silu_approx(acc));
-        dst[t * kDk + c] = y;
-        if (p.dbg)
-          p.dbg[((item * T + t) * 4 + part) * kDk + c] = __float2bfloat16_rn(y);
-        if (RECORD && part == 1)
-          p.rec_kg[(item * T + t) * 2 * kDk + c] = __float2bfloat16_rn(y);
-      }
-      if (sec == 0) {
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          const float y = dst[t * kDk + c];
-          const float sqsum = warp_sum(__fmul_rn(y, y));
-          if (lane == 0) ssum[(t * 2 + s) * 4 + warp] = sqsum;
-        }
+      for (int i = 0; i < 4; ++i) acc = __fmaf_rn(win[t + i], fc.wt[part][i], acc);
+      const float y = bf16_round(silu_approx(acc));
+      dst[t * kDk + c] = y;
+      if (p.dbg) p.dbg[((item * T + t) * 4 + part) * kDk + c] = __float2bfloat16_rn(y);
+      if (RECORD && part == 1)
+        p.rec_kg[(item * T + t) * 2 * kDk + c] = __float2bfloat16_rn(y);
+      if (part < 2) {
+        const float sq = warp_sum(__fmul_rn(y, y));
+        if (lane == 0) ssum[(t * 2 + part) * 4 + fw] = sq;
       }
     }
+  }
 #pragma unroll
-    for (int t = 0; t < T; ++t) gv[t] = bf16_bits_to_float(gate_s[t * kDk + c]);
+  for (int t = 0; t < T; ++t)
+    sv.sg[t * kDk + c] = sigmoid_approx(bf16_bits_to_float(gate_s[t * kDk + c]));
+  if (c < T) {
+    sv.beta[c] = sigmoid_approx(bf16_bits_to_float(dsc.beta_bits[c]));
+    sv.tgt[c] = (T == 1) ? dsc.slot : (RECORD ? 0 : dsc.target[c]);
+  }
+  if (c == 0) sv.meta[0] = n;
 
-    // --- gate projection on tensor cores (KdaWide.kernel, "Gate projection"):
-    // D[feature, token] over 8 rank chunks of 16; token column n = lane/4.
-    {
-      const int g = lane >> 2, q = lane & 3;
-      uint32_t fb0[8], fb1[8];
-      const int ntok = g;
+  // --- gate projection on tensor cores (KdaWide.kernel, "Gate projection"):
+  // D[feature, token] over 8 rank chunks of 16; token column n = lane/4;
+  // warp fw owns features 32fw .. 32fw+31 (two m16 tiles).
+  {
+    const int g = lane >> 2, q = lane & 3;
+    uint32_t fb0[8], fb1[8];
 #pragma unroll
-      for (int kc = 0; kc < 8; ++kc) {
-        if (ntok < T) {
-          const uint2 v =
-              *reinterpret_cast<const uint2 *>(fa_s + ntok * kDk + 16 * kc + 4 * q);
-          fb0[kc] = v.x;
-          fb1[kc] = v.y;
-        } else {
-          fb0[kc] = 0u;
-          fb1[kc] = 0u;
-        }
+    for (int kc = 0; kc < 8; ++kc) {
+      if (g < T) {
+        const uint2 v =
+            *reinterpret_cast<const uint2 *>(fa_s + g * kDk + 16 * kc + 4 * q);
+        fb0[kc] = v.x;
+        fb1[kc] = v.y;
+      } else {
+        fb0[kc] = 0u;
+        fb1[kc] = 0u;
       }
-      float acc[4][4];
+    }
+    // All reads of the stage (and its descriptor) by this thread are done.
+    mbar_arrive(empty_bar);
+    // gate_mode 0: one chain per tile, the two tiles interleaved; gate_mode
+    // 1: four chains of two MMAs per tile, 0 + (((c0 + c1) + c2) + c3).
+    float gv[2][4];
+    if (p.gate_mode == 0) {
+      float acc[2][4];
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
+      for (int m = 0; m < 2; ++m)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[m][e] = 0.0f;
-      if (p.gate_mode == 0) {
 #pragma unroll
-        for (int kc = 0; kc < 8; ++kc) mma_bf16(acc[0], hc.wa[kc], fb0[kc], fb1[kc]);
-      } else {
+      for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+        for (int m = 0; m < 2; ++m) mma_bf16(acc[m], fc.wa[m][kc], fb0[kc], fb1[kc]);
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) gv[m][e] = acc[m][e];
+    } else {
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        float acc[4][4];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[ch][e] = 0.0f;
 #pragma unroll
         for (int kc = 0; kc < 8; ++kc)
-          mma_bf16(acc[kc >> 1], hc.wa[kc], fb0[kc], fb1[kc]);
+          mma_bf16(acc[kc >> 1], fc.wa[m][kc], fb0[kc], fb1[kc]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          gv[m][e] = __fadd_rn(
+              0.0f, __fadd_rn(__fadd_rn(__fadd_rn(acc[0][e], acc[1][e]), acc[2][e]),
+                              acc[3][e]));
       }
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int t = 2 * q + (e & 1);
-        const int f = 16 * warp + g + 8 * (e >> 1);
-        float value = acc[0][e];
-        if (p.gate_mode == 1)
-          value = __fadd_rn(
-              0.0f, __fadd_rn(__fadd_rn(__fadd_rn(value, acc[1][e]), acc[2][e]),
-                              acc[3][e]));
+        const int f = 32 * fw + 16 * m + g + 8 * (e >> 1);
         if (t < T) {
-          const __nv_bfloat16 gb = __float2bfloat16_rn(value);
+          const __nv_bfloat16 gb = __float2bfloat16_rn(gv[m][e]);
           const float raw = __bfloat162float(gb);
           // KdaWide.decay
-          const float z = __fmul_rn(hc.ea, __fadd_rn(raw, hc.dt[e >> 1]));
-          const float dec = exp_approx(__fmul_rn(p.lower_bound, sigmoid_approx(z)));
-          sdec[t * kDk + f] = dec;
+          const float z = __fmul_rn(fc.ea, __fadd_rn(raw, fc.dt[m][e >> 1]));
+          sv.d[t * kDk + f] = exp_approx(__fmul_rn(p.lower_bound, sigmoid_approx(z)));
           if (p.dbg) p.dbg[((item * T + t) * 4 + 3) * kDk + f] = gb;
           if (RECORD) p.rec_kg[(item * T + t) * 2 * kDk + kDk + f] = gb;
         }
       }
     }
-    consumer_sync();
+  }
+  front_sync();
 
-    // --- L2 norms ("Normalized q (with the 1/sqrt(K) scale) and k"),
-    // partial sums combined as KdaWide.quad_sum does.
-    if (sec == 0) {
+  // --- L2 norms ("Normalized q (with the 1/sqrt(K) scale) and k"), partial
+  // sums combined as KdaWide.quad_sum does.
 #pragma unroll
-      for (int t = 0; t < T; ++t) {
-        const float *sq4 = ssum + t * 8;
-        const float qn = __fadd_rn(
-            __fadd_rn(__fadd_rn(sq4[0], sq4[2]), __fadd_rn(sq4[1], sq4[3])), 1.0e-6f);
-        const float kn = __fadd_rn(
-            __fadd_rn(__fadd_rn(sq4[4], sq4[6]), __fadd_rn(sq4[5], sq4[7])), 1.0e-6f);
-        const float fq = rcp_approx(sqrt_approx(qn));
-        const float fk = rcp_approx(sqrt_approx(kn));
-        sq[t * kDk + c] = __fmul_rn(__fmul_rn(sq[t * kDk + c], fq), p.scale);
-        sk[t * kDk + c] = __fmul_rn(sk[t * kDk + c], fk);
-      }
-    }
-    consumer_sync();
+  for (int t = 0; t < T; ++t) {
+    const float *s4 = ssum + t * 8;
+    const float qn =
+        __fadd_rn(__fadd_rn(__fadd_rn(s4[0], s4[2]), __fadd_rn(s4[1], s4[3])), 1.0e-6f);
+    const float kn =
+        __fadd_rn(__fadd_rn(__fadd_rn(s4[4], s4[6]), __fadd_rn(s4[5], s4[7])), 1.0e-6f);
+    const float fq = rcp_approx(sqrt_approx(qn));
+    const float fk = rcp_approx(sqrt_approx(kn));
+    sv.q[t * kDk + c] = __fmul_rn(__fmul_rn(sv.q[t * kDk + c], fq), p.scale);
+    sv.k[t * kDk + c] = __fmul_rn(sv.k[t * kDk + c], fk);
+  }
+}
 
-    // --- recurrence ("The recurrence").  Page rows g + 32m, keys 32c + 4l + e.
-    const int g8 = tid >> 3, l8 = tid & 7;
-    const float *page_s = reinterpret_cast<const float *>(st);
-    float4 S[4][4];
+template <int T, bool RECORD>
+__device__ void front_role(const Params &p, uint8_t *smem, Ctrl *ctl,
+                           const ItemDesc *desc, int n0, int n1) {
+  const int c = threadIdx.x - kRecThreads;  // channel 0..127
+  const int S = p.stages;
+  const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
+  float *ssum = reinterpret_cast<float *>(smem + p.scratch_off);  // [T][2][4]
+  FrontConst fc;
+  int cur_head = -1;
+  int j = 0;  // live items seen
+  for (int k = 0; k < n1 - n0; ++k) {
+    const int stage = k % S;
+    const uint32_t round = static_cast<uint32_t>(k / S);
+    const bool ok = mbar_wait(&ctl->full[stage], round & 1u, &ctl->abort);
+    if (front_sync_or(!ok)) return;
+    const int n = n0 + k;
+    const int h = n / p.batch;
+    const ItemDesc &dsc = desc[stage];
+    if (dsc.status != kLive) {
+      const int r = n - h * p.batch;
+      mbar_arrive(&ctl->empty[stage]);
+#pragma unroll
+      for (int t = 0; t < T; ++t)
+        p.output[(static_cast<int64_t>(r) * T + t) * dim + h * kDk + c] =
+            __float2bfloat16_rn(0.0f);
+      continue;
+    }
+    const int s = j & 1;
+    SlotView<T> sv(smem + p.slot_off + s * p.slot_bytes);
+    if (j >= 2) {
+      // The recurrence has consumed live item j-2's slot.
+      const bool okr = mbar_wait(&ctl->sfree[s], ((j - 2) >> 1) & 1, &ctl->abort);
+      if (front_sync_or(!okr)) return;
+    }
+    if (h != cur_head) {
+      load_front_const(p, h, c, fc);
+      cur_head = h;
+    }
+    front_item<T, RECORD>(p, smem + static_cast<size_t>(stage) * p.stage_bytes, dsc,
+                          n, sv, ssum, fc, c, &ctl->empty[stage]);
+    mbar_arrive(&ctl->fready[s]);
+    ++j;
+  }
+}
+
+// ----------------------------------------------------------------- recurrence
+
+template <int T, bool RECORD>
+__device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
+                                const ItemDesc *desc, int n0, int n1) {
+  const int tid = threadIdx.x;  // 0..255
+  const int lane = tid & 31;
+  const int g8 = tid >> 3, l8 = tid & 7;
+  const int my_row = g8 + 32 * ((l8 >> 1) & 3);
+  const int S = p.stages;
+  const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
+  float *osum = reinterpret_cast<float *>(smem + p.rscratch_off);  // [T][4]
+  // Epilogue mapping: channel ec of token parity et (threads 0-127: even
+  // tokens, 128-255: odd tokens).
+  const int ec = tid & 127, et = tid >> 7, ew = (tid >> 5) & 3;
+  const float nw = bf16_bits_to_float(
+      __ldg(reinterpret_cast<const uint16_t *>(p.norm_weight) + ec));
+  int j = 0;
+  for (int k = 0; k < n1 - n0; ++k) {
+    const int stage = k % S;
+    const uint32_t round = static_cast<uint32_t>(k / S);
+    bool ok = mbar_wait(&ctl->full[stage], round & 1u, &ctl->abort);
+    if (rec_sync_or(!ok)) return;
+    if (desc[stage].status != kLive) {
+      mbar_arrive(&ctl->empty[stage]);
+      continue;
+    }
+    const int n = n0 + k;
+    const int h = n / p.batch;
+    const int r = n - h * p.batch;
+    const int64_t item = static_cast<int64_t>(r) * p.heads + h;
+
+    // The page (rows g8 + 32m, keys 32cc + 4l8 .. +3) into registers.
+    const float *page_s =
+        reinterpret_cast<const float *>(smem + static_cast<size_t>(stage) * p.stage_bytes);
+    float4 S4[4][4];
 #pragma unroll
     for (int m = 0; m < 4; ++m)
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc)
-        S[m][cc] = *reinterpret_cast<const float4 *>(page_s + (g8 + 32 * m) * kDk +
-                                                     32 * cc + 4 * l8);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);  // stage free for the producer
+        S4[m][cc] = *reinterpret_cast<const float4 *>(page_s + (g8 + 32 * m) * kDk +
+                                                      32 * cc + 4 * l8);
+    mbar_arrive(&ctl->empty[stage]);
 
-    const int mrow = (l8 >> 1) & 3;
-    const int my_row = g8 + 32 * mrow;
+    const int s = j & 1;
+    ok = mbar_wait(&ctl->fready[s], (j >> 1) & 1, &ctl->abort);
+    if (rec_sync_or(!ok)) return;
+    SlotView<T> sv(smem + p.slot_off + s * p.slot_bytes);
+
+    // The recurrence ("The recurrence").
 #pragma unroll 1
     for (int t = 0; t < T; ++t) {
-      float4 d4[4], k4[4], q4[4];
+      const float *dt_ = sv.d + t * kDk, *kt = sv.k + t * kDk, *qt = sv.q + t * kDk;
+      float part[4];
+      float2 acc[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) acc[m] = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         const int key = 32 * cc + 4 * l8;
-        d4[cc] = *reinterpret_cast<const float4 *>(sdec + t * kDk + key);
-        k4[cc] = *reinterpret_cast<const float4 *>(sk + t * kDk + key);
-        q4[cc] = *reinterpret_cast<const float4 *>(sq + t * kDk + key);
-      }
-      float part[4];
+        const float4 d4 = *reinterpret_cast<const float4 *>(dt_ + key);
+        const float4 k4 = *reinterpret_cast<const float4 *>(kt + key);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float2 lo = __fmul2_rn(make_float2(S[m][cc].x, S[m][cc].y),
-                                 make_float2(d4[cc].x, d4[cc].y));
-          float2 hi = __fmul2_rn(make_float2(S[m][cc].z, S[m][cc].w),
-                                 make_float2(d4[cc].z, d4[cc].w));
-          S[m][cc] = make_float4(lo.x, lo.y, hi.x, hi.y);
-          a0 = __ffma2_rn(lo, make_float2(k4[cc].x, k4[cc].y), a0);
-          a1 = __ffma2_rn(hi, make_float2(k4[cc].z, k4[cc].w), a1);
+        for (int m = 0; m < 4; ++m) {
+          const float2 lo = __fmul2_rn(make_float2(S4[m][cc].x, S4[m][cc].y),
+                                       make_float2(d4.x, d4.y));
+          const float2 hi = __fmul2_rn(make_float2(S4[m][cc].z, S4[m][cc].w),
+                                       make_float2(d4.z, d4.w));
+          S4[m][cc] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          acc[m] = __ffma2_rn(lo, make_float2(k4.x, k4.y), acc[m]);
+          acc[m] = __ffma2_rn(hi, make_float2(k4.z, k4.w), acc[m]);
         }
-        const float2 a = __fadd2_rn(a0, a1);
-        part[m] = __fadd_rn(a.x, a.y);
       }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) part[m] = __fadd_rn(acc[m].x, acc[m].y);
       const float dot = reduce_scatter8(part, l8);
-      const float u = __fmul_rn(__fsub_rn(sv[t * kDk + my_row], dot), sbeta[t]);
-      if (RECORD && (l8 & 1) == 0)
-        p.rec_u[(item * T + t) * kDk + my_row] = u;
+      const float u = __fmul_rn(__fsub_rn(sv.v[t * kDk + my_row], dot), sv.beta[t]);
+      if (RECORD && (l8 & 1) == 0) p.rec_u[(item * T + t) * kDk + my_row] = u;
       float U[4];
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
-        U[m] = __shfl_sync(0xffffffffu, u, (lane & ~7) | (2 * m));
+      for (int m = 0; m < 4; ++m) U[m] = __shfl_sync(0xffffffffu, u, (lane & ~7) | (2 * m));
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
-        const float2 uu = make_float2(U[m], U[m]);
+      for (int m = 0; m < 4; ++m) acc[m] = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float2 lo = __ffma2_rn(make_float2(k4[cc].x, k4[cc].y), uu,
-                                 make_float2(S[m][cc].x, S[m][cc].y));
-          float2 hi = __ffma2_rn(make_float2(k4[cc].z, k4[cc].w), uu,
-                                 make_float2(S[m][cc].z, S[m][cc].w));
-          S[m][cc] = make_float4(lo.x, lo.y, hi.x, hi.y);
-          a0 = __ffma2_rn(lo, make_float2(q4[cc].x, q4[cc].y), a0);
-          a1 = __ffma2_rn(hi, make_float2(q4[cc].z, q4[cc].w), a1);
+      for (int cc = 0; cc < 4; ++cc) {
+        const int key = 32 * cc + 4 * l8;
+        const float4 k4 = *reinterpret_cast<const float4 *>(kt + key);
+        const float4 q4 = *reinterpret_cast<const float4 *>(qt + key);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float2 uu = make_float2(U[m], U[m]);
+          const float2 lo = __ffma2_rn(make_float2(k4.x, k4.y), uu,
+                                       make_float2(S4[m][cc].x, S4[m][cc].y));
+          const float2 hi = __ffma2_rn(make_float2(k4.z, k4.w), uu,
+                                       make_float2(S4[m][cc].z, S4[m][cc].w));
+          S4[m][cc] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          acc[m] = __ffma2_rn(lo, make_float2(q4.x, q4.y), acc[m]);
+          acc[m] = __ffma2_rn(hi, make_float2(q4.z, q4.w), acc[m]);
         }
-        const float2 a = __fadd2_rn(a0, a1);
-        part[m] = __fadd_rn(a.x, a.y);
       }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) part[m] = __fadd_rn(acc[m].x, acc[m].y);
       const float o = reduce_scatter8(part, l8);
-      if ((l8 & 1) == 0) so[t * kDk + my_row] = bf16_round(o);
+      if ((l8 & 1) == 0) sv.o[t * kDk + my_row] = bf16_round(o);
       if (!RECORD) {
-        const int tgt = target[t];
+        const int tgt = sv.tgt[t];
         if (tgt > 0) {
           float *dstp = p.state + (static_cast<int64_t>(tgt) * p.heads + h) *
                                       static_cast<int64_t>(kDk * kDk);
@@ -731,90 +885,112 @@ __device__ void consumer(const Params &p, uint8_t *smem, uint64_t *full,
             for (int cc = 0; cc < 4; ++cc)
               __stcs(reinterpret_cast<float4 *>(dstp + (g8 + 32 * m) * kDk + 32 * cc +
                                                 4 * l8),
-                     S[m][cc]);
+                     S4[m][cc]);
         }
       }
     }
-    consumer_sync();
+    rec_sync();
 
-    // --- gated RMSNorm epilogue ("Gated RMSNorm"), threads 0-127: channel c.
-    float ov[T];
-    if (sec == 0) {
+    // --- gated RMSNorm epilogue ("Gated RMSNorm"), partial sums of the four
+    // warps of a token combined as KdaWide.quad_sum does.
+    float ov[(T + 1) / 2];
 #pragma unroll
-      for (int t = 0; t < T; ++t) {
-        ov[t] = so[t * kDk + c];
-        const float tot = warp_sum(__fmul_rn(ov[t], ov[t]));
-        if (lane == 0) osum[t * 4 + warp] = tot;
+    for (int i = 0; i < (T + 1) / 2; ++i) {
+      const int t = 2 * i + et;
+      if (t < T) {
+        ov[i] = sv.o[t * kDk + ec];
+        const float tot = warp_sum(__fmul_rn(ov[i], ov[i]));
+        if (lane == 0) osum[t * 4 + ew] = tot;
       }
     }
-    consumer_sync();
-    if (sec == 0) {
+    rec_sync();
 #pragma unroll
-      for (int t = 0; t < T; ++t) {
+    for (int i = 0; i < (T + 1) / 2; ++i) {
+      const int t = 2 * i + et;
+      if (t < T) {
         const float *o4 = osum + t * 4;
         const float sumsq =
             __fadd_rn(__fadd_rn(o4[0], o4[2]), __fadd_rn(o4[1], o4[3]));
         const float var = __fadd_rn(__fmul_rn(sumsq, 1.0f / 128.0f), p.eps);
         const float rstd = rcp_approx(sqrt_approx(var));
-        const float y = __fmul_rn(__fmul_rn(__fmul_rn(ov[t], rstd), nw),
-                                  sigmoid_approx(gv[t]));
-        p.output[(static_cast<int64_t>(r) * T + t) * dim + h * kDk + c] =
+        const float y =
+            __fmul_rn(__fmul_rn(__fmul_rn(ov[i], rstd), nw), sv.sg[t * kDk + ec]);
+        p.output[(static_cast<int64_t>(r) * T + t) * dim + h * kDk + ec] =
             __float2bfloat16_rn(y);
       }
     }
+    mbar_arrive(&ctl->sfree[s]);
+    ++j;
   }
 }
 
 template <int T, bool RECORD>
 __global__ void __launch_bounds__(kThreads, 1) kda_step_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);
-  uint64_t *empty = full + kMaxStages;
+  Ctrl *ctl = reinterpret_cast<Ctrl *>(smem + p.bar_off);
   ItemDesc *desc = reinterpret_cast<ItemDesc *>(smem + p.desc_off);
   const int G = gridDim.x;
   const int n0 = static_cast<int>((static_cast<int64_t>(p.items) * blockIdx.x) / G);
   const int n1 = static_cast<int>((static_cast<int64_t>(p.items) * (blockIdx.x + 1)) / G);
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumers / 32);
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], kRecThreads + kFrontThreads);
     }
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&ctl->fready[s], kFrontThreads);
+      mbar_init(&ctl->sfree[s], kRecThreads);
+    }
+    ctl->abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (threadIdx.x >= kConsumers) {
-    if (threadIdx.x == kConsumers)
-      producer<T, RECORD>(p, smem, full, empty, desc, n0, n1);
-    return;
+  if (threadIdx.x < kRecThreads) {
+    regs_inc<kRecRegs>();
+    recurrence_role<T, RECORD>(p, smem, ctl, desc, n0, n1);
+  } else if (threadIdx.x < kProducer) {
+    regs_inc<kFrontRegs>();
+    front_role<T, RECORD>(p, smem, ctl, desc, n0, n1);
+  } else {
+    regs_dec<kProducerRegs>();
+    if (threadIdx.x == kProducer) producer_role<T, RECORD>(p, smem, ctl, desc, n0, n1);
   }
-  consumer<T, RECORD>(p, smem, full, empty, desc, n0, n1);
 }
 
 // ------------------------------------------------------------------ host side
 
 struct Layout {
   uint32_t stage_bytes, conv_off, x_off, gate_off, fa_off;
-  uint32_t bar_off, desc_off, front_off, total;
+  uint32_t bar_off, desc_off, slot_off, slot_bytes, scratch_off, rscratch_off, total;
   int stages;
 };
 
 static uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
+// Stage: page | conv rows (3 x 128 x W bf16) | x (T x 3 x 128) | gate | f_a.
+// Then the control block, the item descriptors, two hand-off slots and the
+// front's partial-sum scratch.  Three stages when they fit, else two.
 static bool make_layout(int T, int W, int max_smem, Layout &L) {
   L.conv_off = kPageBytes;
   L.x_off = align_up(L.conv_off + 3u * 256u * W, 128);
   L.gate_off = L.x_off + 3u * T * 256u;
   L.fa_off = L.gate_off + T * 256u;
   L.stage_bytes = align_up(L.fa_off + T * 256u, 128);
-  const uint32_t tail = 2 * kMaxStages * 8 + kMaxStages * sizeof(ItemDesc) +
-                        (5u * T * kDk + 8 + T * 8 + T * 4) * 4;
+  L.slot_bytes = align_up((6u * T * kDk + 2u * KDA_MAX_TOKENS + 4u) * 4u, 128);
+  const uint32_t ctrl = align_up(sizeof(Ctrl), 128);
+  const uint32_t descs = align_up(kMaxStages * sizeof(ItemDesc), 128);
+  const uint32_t scratch = align_up(T * 8u * 4u, 128);   // front q/k square sums
+  const uint32_t rscratch = align_up(T * 4u * 4u, 128);  // recurrence o square sums
+  const uint32_t tail = ctrl + descs + kSlots * L.slot_bytes + scratch + rscratch;
   for (int s = kMaxStages; s >= 2; --s) {
     const uint32_t total = s * L.stage_bytes + tail;
     if (total <= static_cast<uint32_t>(max_smem)) {
       L.stages = s;
       L.bar_off = s * L.stage_bytes;
-      L.desc_off = L.bar_off + 2 * kMaxStages * 8;
-      L.front_off = L.desc_off + kMaxStages * sizeof(ItemDesc);
+      L.desc_off = L.bar_off + ctrl;
+      L.slot_off = L.desc_off + descs;
+      L.scratch_off = L.slot_off + kSlots * L.slot_bytes;
+      L.rscratch_off = L.scratch_off + scratch;
       L.total = total;
       return true;
     }
@@ -930,7 +1106,10 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
   prm.fa_off = L.fa_off;
   prm.bar_off = L.bar_off;
   prm.desc_off = L.desc_off;
-  prm.front_off = L.front_off;
+  prm.slot_off = L.slot_off;
+  prm.slot_bytes = L.slot_bytes;
+  prm.scratch_off = L.scratch_off;
+  prm.rscratch_off = L.rscratch_off;
   prm.x = static_cast<const __nv_bfloat16 *>(a->x);
   prm.conv_weight = static_cast<const __nv_bfloat16 *>(a->conv_weight);
   prm.conv_bias = static_cast<const __nv_bfloat16 *>(a->has_bias ? a->conv_bias : a->conv_weight);
