@@ -25,9 +25,17 @@
 //                  registers: thread (g = tid/8, l = tid%8) holds keys
 //                  {32c + 4l + e} of value rows g, g+32, g+64, g+96 (64
 //                  floats), packed FP32 (f32x2) multiplies/FMAs, row sums by an
-//                  8-lane reduce-scatter; the page goes from registers to HBM
-//                  with 16-byte streaming stores after every token; then the
-//                  gated RMSNorm epilogue of the item.
+//                  8-lane reduce-scatter; then the gated RMSNorm epilogue.
+//                  Updated pages leave shared memory through TMA bulk stores,
+//                  so no per-thread global stores queue in L1TEX:
+//                  decode: the page goes, one 16 KiB quarter (32 rows) at a
+//                  time, into a ring of quarter buffers served by
+//       store      (warpgroup 3, one thread), which bulk-stores each quarter
+//                  and frees its buffer once the copy has read it; the stage
+//                  is refilled as soon as the page is in registers;
+//                  verify: after each written token the page goes back into
+//                  its stage buffer and the recurrence leader bulk-stores it;
+//                  the stage is released after the last store has read it.
 //     The time per item is max(front, recurrence), not their sum.
 //   * setmaxnreg moves registers from the producer warpgroup (40 a thread) to
 //     the recurrence (160) and front (144) warpgroups; launch gives 128.
@@ -45,6 +53,7 @@ constexpr int kDk = 128;                          // dk = dv = gate rank
 constexpr int kRecThreads = 256;                  // warpgroups 0-1
 constexpr int kFrontThreads = 128;                // warpgroup 2
 constexpr int kProducer = kRecThreads + kFrontThreads;  // warpgroup 3, thread 0
+constexpr int kStorer = kProducer + 32;                 // warpgroup 3, warp 1 lane 0
 constexpr int kThreads = kProducer + 128;
 constexpr int kRecRegs = 160;                     // setmaxnreg split (launch: 128)
 constexpr int kFrontRegs = 144;
@@ -52,6 +61,8 @@ constexpr int kProducerRegs = 40;
 constexpr uint32_t kPageBytes = kDk * kDk * 4;
 constexpr int kMaxStages = 3;
 constexpr int kSlots = 2;                         // front -> recurrence hand-off
+constexpr int kMaxQuarterBufs = 4;                // 16 KiB quarter-page store ring
+constexpr uint32_t kQuarterBytes = kPageBytes / 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kLive = 0, kPad = 1, kError = 2;
 
@@ -73,6 +84,8 @@ struct Params {
   int32_t items, stages;
   uint32_t stage_bytes, conv_off, x_off, gate_off, fa_off;
   uint32_t bar_off, desc_off, slot_off, slot_bytes, scratch_off, rscratch_off;
+  uint32_t qbuf_off;
+  int32_t nqbuf;
   const __nv_bfloat16 *x, *conv_weight, *conv_bias, *f_a, *f_b, *beta, *gate,
       *norm_weight;
   const float *a_log, *dt_bias;
@@ -93,6 +106,10 @@ struct Ctrl {
   uint64_t empty[kMaxStages];  // front + recurrence -> producer (stage free)
   uint64_t fready[kSlots];     // front -> recurrence (slot inputs written)
   uint64_t sfree[kSlots];      // recurrence -> front (slot consumed)
+  uint64_t qready[kMaxQuarterBufs];  // recurrence -> store (quarter written)
+  uint64_t qfree[kMaxQuarterBufs];   // store -> recurrence (quarter read out)
+  float *qdst[kMaxQuarterBufs];      // HBM destination of each quarter, or null
+                                     // to end the store thread's loop
   uint32_t abort;
 };
 
@@ -134,6 +151,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   asm volatile(
       "{\n .reg .pred p;\n"
       " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of the phase of `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity)
@@ -203,6 +233,39 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src,
       ".L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
+}
+
+// TMA bulk copy of this CTA's shared memory -> global, tracked as a bulk
+// group of the issuing thread.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
+          dst),
+      "r"(smem_addr(src)), "r"(bytes), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until at most `pending` committed bulk stores are still reading
+// shared memory (0..3).
+__device__ __forceinline__ void bulk_wait_read(int pending) {
+  switch (pending) {
+    case 3: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); break;
+    default: asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); break;
+  }
+}
+// Waits until every committed bulk store is complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Named barrier 1 over the 256 recurrence threads.
@@ -329,22 +392,24 @@ __device__ __forceinline__ float reduce_scatter8(const float (&x)[4], int l) {
 }
 
 // Hand-off slot between the front and the recurrence (one per live item in
-// flight): FP32 [T][128] arrays and the item's scalars.
+// flight): FP32 [T][128] q_hat, k_hat, decay; BF16 [T][128] v, gate, o (all
+// three are BF16 values, so the bits move unchanged); beta, targets, item.
 template <int T>
 struct SlotView {
-  float *q, *k, *d, *v, *sg, *o, *beta;
+  float *q, *k, *d, *beta;
+  uint16_t *v, *gate, *o;
   int32_t *tgt, *meta;
   __device__ __forceinline__ explicit SlotView(uint8_t *base) {
     float *f = reinterpret_cast<float *>(base);
     q = f;
     k = q + T * kDk;
     d = k + T * kDk;
-    v = d + T * kDk;
-    sg = v + T * kDk;
-    o = sg + T * kDk;
-    beta = o + T * kDk;
+    beta = d + T * kDk;
     tgt = reinterpret_cast<int32_t *>(beta + KDA_MAX_TOKENS);
     meta = tgt + KDA_MAX_TOKENS;
+    v = reinterpret_cast<uint16_t *>(meta + 4);
+    gate = v + T * kDk;
+    o = gate + T * kDk;
   }
 };
 
@@ -608,14 +673,15 @@ __device__ __forceinline__ void front_item(const Params &p, const uint8_t *st,
     crow[1] = tap2;
 #pragma unroll
     for (int t = 0; t < T; ++t) crow[2 + t] = xb[t];
-    float *dst = part == 0 ? sv.q : (part == 1 ? sv.k : sv.v);
 #pragma unroll
     for (int t = 0; t < T; ++t) {
       float acc = fc.bias[part];
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc = __fmaf_rn(win[t + i], fc.wt[part][i], acc);
       const float y = bf16_round(silu_approx(acc));
-      dst[t * kDk + c] = y;
+      if (part == 0) sv.q[t * kDk + c] = y;
+      else if (part == 1) sv.k[t * kDk + c] = y;
+      else sv.v[t * kDk + c] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
       if (p.dbg) p.dbg[((item * T + t) * 4 + part) * kDk + c] = __float2bfloat16_rn(y);
       if (RECORD && part == 1)
         p.rec_kg[(item * T + t) * 2 * kDk + c] = __float2bfloat16_rn(y);
@@ -626,8 +692,7 @@ __device__ __forceinline__ void front_item(const Params &p, const uint8_t *st,
     }
   }
 #pragma unroll
-  for (int t = 0; t < T; ++t)
-    sv.sg[t * kDk + c] = sigmoid_approx(bf16_bits_to_float(gate_s[t * kDk + c]));
+  for (int t = 0; t < T; ++t) sv.gate[t * kDk + c] = gate_s[t * kDk + c];
   if (c < T) {
     sv.beta[c] = sigmoid_approx(bf16_bits_to_float(dsc.beta_bits[c]));
     sv.tgt[c] = (T == 1) ? dsc.slot : (RECORD ? 0 : dsc.target[c]);
@@ -787,14 +852,19 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
   const int ec = tid & 127, et = tid >> 7, ew = (tid >> 5) & 3;
   const float nw = bf16_bits_to_float(
       __ldg(reinterpret_cast<const uint16_t *>(p.norm_weight) + ec));
+  const uint64_t pol = policy_evict_first();
   int j = 0;
+  uint32_t wq = 0;  // decode: quarters handed to the store thread so far
   for (int k = 0; k < n1 - n0; ++k) {
     const int stage = k % S;
     const uint32_t round = static_cast<uint32_t>(k / S);
     bool ok = mbar_wait(&ctl->full[stage], round & 1u, &ctl->abort);
-    if (rec_sync_or(!ok)) return;
+    if (rec_sync_or(!ok)) {
+      if (T > 1 && !RECORD && tid == 0) bulk_wait_all();
+      return;
+    }
     if (desc[stage].status != kLive) {
-      mbar_arrive(&ctl->empty[stage]);
+      if (tid == 0) mbar_arrive(&ctl->empty[stage]);
       continue;
     }
     const int n = n0 + k;
@@ -803,8 +873,8 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
     const int64_t item = static_cast<int64_t>(r) * p.heads + h;
 
     // The page (rows g8 + 32m, keys 32cc + 4l8 .. +3) into registers.
-    const float *page_s =
-        reinterpret_cast<const float *>(smem + static_cast<size_t>(stage) * p.stage_bytes);
+    float *page_s =
+        reinterpret_cast<float *>(smem + static_cast<size_t>(stage) * p.stage_bytes);
     float4 S4[4][4];
 #pragma unroll
     for (int m = 0; m < 4; ++m)
@@ -812,11 +882,18 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
       for (int cc = 0; cc < 4; ++cc)
         S4[m][cc] = *reinterpret_cast<const float4 *>(page_s + (g8 + 32 * m) * kDk +
                                                       32 * cc + 4 * l8);
-    mbar_arrive(&ctl->empty[stage]);
+    rec_sync();
+    // Page loaded: decode and record steps free the stage now; verify steps
+    // reuse it as the store buffer of the written pages.
+    if ((T == 1 || RECORD) && tid == 0) mbar_arrive(&ctl->empty[stage]);
+    bool stored = false;
 
     const int s = j & 1;
     ok = mbar_wait(&ctl->fready[s], (j >> 1) & 1, &ctl->abort);
-    if (rec_sync_or(!ok)) return;
+    if (rec_sync_or(!ok)) {
+      if (T > 1 && !RECORD && tid == 0) bulk_wait_all();
+      return;
+    }
     SlotView<T> sv(smem + p.slot_off + s * p.slot_bytes);
 
     // The recurrence ("The recurrence").
@@ -846,7 +923,8 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
 #pragma unroll
       for (int m = 0; m < 4; ++m) part[m] = __fadd_rn(acc[m].x, acc[m].y);
       const float dot = reduce_scatter8(part, l8);
-      const float u = __fmul_rn(__fsub_rn(sv.v[t * kDk + my_row], dot), sv.beta[t]);
+      const float u = __fmul_rn(
+          __fsub_rn(bf16_bits_to_float(sv.v[t * kDk + my_row]), dot), sv.beta[t]);
       if (RECORD && (l8 & 1) == 0) p.rec_u[(item * T + t) * kDk + my_row] = u;
       float U[4];
 #pragma unroll
@@ -873,19 +951,57 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
 #pragma unroll
       for (int m = 0; m < 4; ++m) part[m] = __fadd_rn(acc[m].x, acc[m].y);
       const float o = reduce_scatter8(part, l8);
-      if ((l8 & 1) == 0) sv.o[t * kDk + my_row] = bf16_round(o);
+      if ((l8 & 1) == 0)
+        sv.o[t * kDk + my_row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
       if (!RECORD) {
         const int tgt = sv.tgt[t];
         if (tgt > 0) {
-          float *dstp = p.state + (static_cast<int64_t>(tgt) * p.heads + h) *
-                                      static_cast<int64_t>(kDk * kDk);
+          float *page_g = p.state + (static_cast<int64_t>(tgt) * p.heads + h) *
+                                        static_cast<int64_t>(kDk * kDk);
+          if (T == 1) {
+            // Quarter m = value rows 32m .. 32m+31 = this thread's row g8 + 32m.
 #pragma unroll
-          for (int m = 0; m < 4; ++m)
+            for (int m = 0; m < 4; ++m) {
+              const int b = static_cast<int>(wq % static_cast<uint32_t>(p.nqbuf));
+              const uint32_t use = wq / static_cast<uint32_t>(p.nqbuf);
+              if (use > 0) {
+                ok = mbar_wait(&ctl->qfree[b], (use - 1u) & 1u, &ctl->abort);
+                if (rec_sync_or(!ok)) return;
+              }
+              float *qb =
+                  reinterpret_cast<float *>(smem + p.qbuf_off + b * kQuarterBytes);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-              __stcs(reinterpret_cast<float4 *>(dstp + (g8 + 32 * m) * kDk + 32 * cc +
-                                                4 * l8),
-                     S4[m][cc]);
+              for (int cc = 0; cc < 4; ++cc)
+                *reinterpret_cast<float4 *>(qb + g8 * kDk + 32 * cc + 4 * l8) =
+                    S4[m][cc];
+              fence_proxy_async_smem();
+              rec_sync();
+              if (tid == 0) {
+                ctl->qdst[b] = page_g + m * (kQuarterBytes / 4);
+                mbar_arrive(&ctl->qready[b]);
+              }
+              ++wq;
+            }
+          } else {
+            // The stage buffer may still be read by the previous token's store.
+            if (stored) {
+              if (tid == 0) bulk_wait_read(0);
+              rec_sync();
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+                *reinterpret_cast<float4 *>(page_s + (g8 + 32 * m) * kDk + 32 * cc +
+                                            4 * l8) = S4[m][cc];
+            fence_proxy_async_smem();
+            rec_sync();
+            if (tid == 0) {
+              bulk_s2g(page_g, page_s, kPageBytes, pol);
+              bulk_commit();
+            }
+            stored = true;
+          }
         }
       }
     }
@@ -898,7 +1014,7 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
     for (int i = 0; i < (T + 1) / 2; ++i) {
       const int t = 2 * i + et;
       if (t < T) {
-        ov[i] = sv.o[t * kDk + ec];
+        ov[i] = bf16_bits_to_float(sv.o[t * kDk + ec]);
         const float tot = warp_sum(__fmul_rn(ov[i], ov[i]));
         if (lane == 0) osum[t * 4 + ew] = tot;
       }
@@ -913,15 +1029,65 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
             __fadd_rn(__fadd_rn(o4[0], o4[2]), __fadd_rn(o4[1], o4[3]));
         const float var = __fadd_rn(__fmul_rn(sumsq, 1.0f / 128.0f), p.eps);
         const float rstd = rcp_approx(sqrt_approx(var));
-        const float y =
-            __fmul_rn(__fmul_rn(__fmul_rn(ov[i], rstd), nw), sv.sg[t * kDk + ec]);
+        const float sg = sigmoid_approx(bf16_bits_to_float(sv.gate[t * kDk + ec]));
+        const float y = __fmul_rn(__fmul_rn(__fmul_rn(ov[i], rstd), nw), sg);
         p.output[(static_cast<int64_t>(r) * T + t) * dim + h * kDk + ec] =
             __float2bfloat16_rn(y);
       }
     }
     mbar_arrive(&ctl->sfree[s]);
+    if (T > 1 && !RECORD && tid == 0) {
+      bulk_wait_read(0);
+      mbar_arrive(&ctl->empty[stage]);
+    }
     ++j;
   }
+  if (T > 1 && !RECORD && tid == 0) bulk_wait_all();
+  if (T == 1) {
+    // End of stream for the store thread.
+    const int b = static_cast<int>(wq % static_cast<uint32_t>(p.nqbuf));
+    const uint32_t use = wq / static_cast<uint32_t>(p.nqbuf);
+    if (use > 0) {
+      const bool ok = mbar_wait(&ctl->qfree[b], (use - 1u) & 1u, &ctl->abort);
+      if (rec_sync_or(!ok)) return;
+    }
+    if (tid == 0) {
+      ctl->qdst[b] = nullptr;
+      mbar_arrive(&ctl->qready[b]);
+    }
+  }
+}
+
+// ----------------------------------------------------------------- store
+
+// Serves the quarter ring in order.  Quarter #q sits in buffer q % n.  The
+// loop issues the next quarter as soon as the recurrence has written it;
+// otherwise it retires the oldest store in flight (waits until that copy has
+// read shared memory) and frees its buffer; with nothing in flight it sleeps
+// until the next quarter.  A null destination ends the stream.
+__device__ void store_role(const Params &p, uint8_t *smem, Ctrl *ctl) {
+  const uint64_t pol = policy_evict_first();
+  const uint32_t n = static_cast<uint32_t>(p.nqbuf);
+  uint32_t issued = 0, freed = 0;
+  for (;;) {
+    const int b = static_cast<int>(issued % n);
+    const uint32_t par = (issued / n) & 1u;
+    if (mbar_test_wait(&ctl->qready[b], par)) {
+      float *dst = ctl->qdst[b];
+      if (dst == nullptr) break;
+      bulk_s2g(dst, smem + p.qbuf_off + b * kQuarterBytes, kQuarterBytes, pol);
+      bulk_commit();
+      ++issued;
+    } else if (issued > freed) {
+      const uint32_t pending = issued - freed;
+      bulk_wait_read(static_cast<int>(pending > 4u ? 3u : pending - 1u));
+      mbar_arrive(&ctl->qfree[freed % n]);
+      ++freed;
+    } else if (!mbar_wait(&ctl->qready[b], par, &ctl->abort)) {
+      break;
+    }
+  }
+  bulk_wait_all();
 }
 
 template <int T, bool RECORD>
@@ -935,11 +1101,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_step_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], kRecThreads + kFrontThreads);
+      mbar_init(&ctl->empty[s], 1 + kFrontThreads);  // front, recurrence
     }
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&ctl->fready[s], kFrontThreads);
       mbar_init(&ctl->sfree[s], kRecThreads);
+    }
+    for (int b = 0; b < kMaxQuarterBufs; ++b) {
+      mbar_init(&ctl->qready[b], 1);
+      mbar_init(&ctl->qfree[b], 1);
     }
     ctl->abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -954,6 +1124,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_step_kernel(const __grid_cons
   } else {
     regs_dec<kProducerRegs>();
     if (threadIdx.x == kProducer) producer_role<T, RECORD>(p, smem, ctl, desc, n0, n1);
+    if (T == 1 && threadIdx.x == kStorer) store_role(p, smem, ctl);
   }
 }
 
@@ -961,32 +1132,42 @@ __global__ void __launch_bounds__(kThreads, 1) kda_step_kernel(const __grid_cons
 
 struct Layout {
   uint32_t stage_bytes, conv_off, x_off, gate_off, fa_off;
-  uint32_t bar_off, desc_off, slot_off, slot_bytes, scratch_off, rscratch_off, total;
-  int stages;
+  uint32_t bar_off, desc_off, slot_off, slot_bytes, scratch_off, rscratch_off;
+  uint32_t qbuf_off, total;
+  int stages, nqbuf;
 };
 
 static uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 // Stage: page | conv rows (3 x 128 x W bf16) | x (T x 3 x 128) | gate | f_a.
-// Then the control block, the item descriptors, two hand-off slots and the
-// front's partial-sum scratch.  Three stages when they fit, else two.
-static bool make_layout(int T, int W, int max_smem, Layout &L) {
+// Then the quarter-page store ring, the control block, item descriptors, two
+// hand-off slots and the partial-sum scratch.  Decode uses two stages and as
+// many 16 KiB quarter buffers (up to 4) as fit; verify and record steps take
+// three stages when they fit, else two.
+static bool make_layout(int T, int W, bool record, int max_smem, Layout &L) {
   L.conv_off = kPageBytes;
   L.x_off = align_up(L.conv_off + 3u * 256u * W, 128);
   L.gate_off = L.x_off + 3u * T * 256u;
   L.fa_off = L.gate_off + T * 256u;
   L.stage_bytes = align_up(L.fa_off + T * 256u, 128);
-  L.slot_bytes = align_up((6u * T * kDk + 2u * KDA_MAX_TOKENS + 4u) * 4u, 128);
+  L.slot_bytes = align_up((3u * T * kDk + 2u * KDA_MAX_TOKENS + 4u) * 4u +
+                              3u * T * kDk * 2u,
+                          128);
   const uint32_t ctrl = align_up(sizeof(Ctrl), 128);
   const uint32_t descs = align_up(kMaxStages * sizeof(ItemDesc), 128);
   const uint32_t scratch = align_up(T * 8u * 4u, 128);   // front q/k square sums
   const uint32_t rscratch = align_up(T * 4u * 4u, 128);  // recurrence o square sums
-  const uint32_t tail = ctrl + descs + kSlots * L.slot_bytes + scratch + rscratch;
-  for (int s = kMaxStages; s >= 2; --s) {
-    const uint32_t total = s * L.stage_bytes + tail;
-    if (total <= static_cast<uint32_t>(max_smem)) {
+  const uint32_t fixed = ctrl + descs + kSlots * L.slot_bytes + scratch + rscratch;
+  const bool ring = T == 1 && !record;
+  const int s_max = ring ? 2 : kMaxStages;
+  for (int s = s_max; s >= 2; --s) {
+    for (int nq = ring ? kMaxQuarterBufs : 0; nq >= (ring ? 1 : 0); --nq) {
+      const uint32_t total = s * L.stage_bytes + fixed + nq * kQuarterBytes;
+      if (total > static_cast<uint32_t>(max_smem)) continue;
       L.stages = s;
-      L.bar_off = s * L.stage_bytes;
+      L.nqbuf = nq;
+      L.qbuf_off = s * L.stage_bytes;
+      L.bar_off = L.qbuf_off + nq * kQuarterBytes;
       L.desc_off = L.bar_off + ctrl;
       L.slot_off = L.desc_off + descs;
       L.scratch_off = L.slot_off + kSlots * L.slot_bytes;
@@ -1087,7 +1268,8 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
     di.ok = true;
   }
   Layout L;
-  if (!make_layout(T, a->conv_width, di.max_smem, L)) return KDA_ERR_CONV_WIDTH;
+  if (!make_layout(T, a->conv_width, a->record != 0, di.max_smem, L))
+    return KDA_ERR_CONV_WIDTH;
 
   Params prm;
   prm.batch = a->batch;
@@ -1110,6 +1292,8 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
   prm.slot_bytes = L.slot_bytes;
   prm.scratch_off = L.scratch_off;
   prm.rscratch_off = L.rscratch_off;
+  prm.qbuf_off = L.qbuf_off;
+  prm.nqbuf = L.nqbuf;
   prm.x = static_cast<const __nv_bfloat16 *>(a->x);
   prm.conv_weight = static_cast<const __nv_bfloat16 *>(a->conv_weight);
   prm.conv_bias = static_cast<const __nv_bfloat16 *>(a->has_bias ? a->conv_bias : a->conv_weight);
