@@ -547,14 +547,26 @@ __device__ void producer_role(const Params &p, uint8_t *smem, Ctrl *ctl,
   for (int k = pro; k < count; ++k) {
     const int stage = k % S;
     const uint32_t round = static_cast<uint32_t>(k / S);
+    // Verify items resolve their slots (dependent global loads) while the
+    // stage is still busy; decode items after the wait (measured faster).
+    ItemDesc nd;
+    int flags = 0;
+    if (T > 1) {
+      flags = resolve_item<T, RECORD>(p, n0 + k, nd);
+      load_beta<T>(p, n0 + k, nd);
+    }
     if (!mbar_wait(&ctl->empty[stage], (round - 1u) & 1u, &ctl->abort)) {
       aborted = true;
       break;
     }
     ItemDesc &d = desc[stage];
-    const int flags = resolve_item<T, RECORD>(p, n0 + k, d);
+    if (T > 1) {
+      d = nd;
+    } else {
+      flags = resolve_item<T, RECORD>(p, n0 + k, d);
+      load_beta<T>(p, n0 + k, d);
+    }
     if (flags && p.err) atomicOr(p.err, flags);
-    load_beta<T>(p, n0 + k, d);
     uint8_t *st = smem + static_cast<size_t>(stage) * p.stage_bytes;
     if (d.status == kLive) {
       mbar_arrive_expect_tx(&ctl->full[stage], kPageBytes + small_bytes<T>(p));
