@@ -48,6 +48,19 @@ def dist_env():
     return rank, world, local
 
 
+def shard_workload(workload, rank: int):
+    """Rank r's batch: same shape, its own seed (independent requests)."""
+    return workload.with_(seed=workload.seed + 7919 * rank)
+
+
+def max_over_ranks(values, dist, device):
+    """Element-wise max of a list of floats over all ranks (timing only)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -235,7 +248,7 @@ def main():
     from linear_attention_recurrent_kda_gb300.api import step_from_inputs
     from linear_attention_recurrent_kda_gb300.workloads import make_inputs
 
-    w = workload.with_(seed=workload.seed + 7919 * rank)
+    w = shard_workload(workload, rank)
     host = make_inputs(w)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
     B, H, T = w.batch, w.heads, w.tokens
@@ -289,9 +302,7 @@ def main():
     kern_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
     ms_step = total_ms / args.steps
     if pg is not None:
-        t = torch.tensor([ms_step, kern_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_step, kern_ms = float(t[0]), float(t[1])
+        ms_step, kern_ms = max_over_ranks([ms_step, kern_ms], pg, dev)
     clocks = sampler.summary(t_host0 - 0.15, t_host1 + 0.15)
     clock_window = "timed"
     if clocks is None:
@@ -325,9 +336,7 @@ def main():
         torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if pg is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+        (e2e_ms,) = max_over_ranks([e2e_ms], pg, dev)
 
     items = w.items * world
     value = items / (ms_step * 1e-3)
