@@ -134,6 +134,40 @@ int kda_decode(const kda_args *args, void *stream);
 /* One speculative-verify step (tokens 2..8, record optional) on `stream`. */
 int kda_verify(const kda_args *args, void *stream);
 
+/* Arguments of one record replay (kda_recover). */
+typedef struct kda_recover_args {
+  int32_t batch;            /* B requests (0 is a no-op)                       */
+  int32_t heads;            /* H heads (0 is a no-op)                          */
+  int32_t tokens;           /* T of the records, 1..8                          */
+  int32_t num_slots;        /* slots in the state pool                         */
+  const int32_t *src_slots; /* i32 [B]: checkpoint page; <= 0 = padding        */
+  const int32_t *dst_slots; /* i32 [B]: page to write; <= 0 = padding; may     */
+                            /* equal src_slots[r]                              */
+  const int32_t *accepted;  /* i32 [B]: tokens to replay, 0..T (0 = copy)      */
+  const float *rec_u;       /* f32 [B, H, T, 128] from a record-mode verify    */
+  const void *rec_kg;       /* bf16 [B, H, T, 256]: k (pre-norm) | raw_g       */
+  const float *a_log;       /* f32 [H]                                         */
+  const float *dt_bias;     /* f32 [H*128]                                     */
+  float lower_bound;        /* as in the step that wrote the records           */
+  float *state;             /* f32 [num_slots, H, 128, 128]       in/out       */
+  int32_t *err;             /* optional device word for KDA_DEVERR_* flags     */
+} kda_recover_args;
+
+/* Record replay ("RecoverSSM" on the page, referenced but not shown there).
+ * A record-mode kda_verify writes no state; it leaves per token the BF16 k
+ * before the L2 norm, the BF16 raw gate and the FP32 u of every value row.
+ * For each (request r, head h): start from state[src_slots[r], h], for the
+ * first accepted[r] tokens decay every key column by the decay of the
+ * recorded raw gate and add k_hat u^T (k_hat: L2-normalised recorded k), and
+ * write the page to state[dst_slots[r], h].  The arithmetic is the step's, so
+ * replaying the records of a record-mode verify reproduces bit for bit the
+ * page a non-record verify writes after token accepted[r]-1.
+ * Pointers are device pointers; state, rec_u and rec_kg need 16-byte
+ * alignment.  Slot >= num_slots or accepted outside 0..T raise
+ * KDA_DEVERR_SLOT / KDA_DEVERR_ACCEPTED and the item writes nothing.  Pages
+ * of different requests must be distinct.  One kernel on `stream`. */
+int kda_recover(const kda_recover_args *args, void *stream);
+
 /* Static description of a return code (never NULL). */
 const char *kda_strerror(int code);
 

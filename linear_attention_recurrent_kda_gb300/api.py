@@ -169,3 +169,37 @@ def step_from_inputs(dev_inputs: Dict[str, object], output: torch.Tensor, *,
         conv_bias=d.get("conv_bias") if d.get("has_bias") else None,
         gate_mode=int(d["gate_mode"]), record=bool(d["record"]), rec_u=rec_u,
         rec_kg=rec_kg, err=err, dbg=dbg, use_pdl=use_pdl)
+
+
+def kda_recover(*, state, src_slots, dst_slots, accepted, rec_u, rec_kg, a_log,
+                dt_bias, lower_bound: float, err=None,
+                stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Record replay (include/kda.h ``kda_recover``): rebuild the accepted
+    state pages from checkpoint pages and a record-mode verify's records."""
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    _check("rec_u", rec_u, f32)
+    if rec_u.dim() != 4 or rec_u.shape[3] != DK:
+        raise ValueError("rec_u must be [batch, heads, tokens, 128]")
+    B, H, T = rec_u.shape[:3]
+    _check("rec_kg", rec_kg, bf, (B, H, T, 2 * DK))
+    _check("state", state, f32)
+    if state.dim() != 4 or tuple(state.shape[1:]) != (H, DK, DK):
+        raise ValueError("state must be [num_slots, heads, 128, 128]")
+    for n, t in (("src_slots", src_slots), ("dst_slots", dst_slots),
+                 ("accepted", accepted)):
+        _check(n, t, i32, (B,))
+    _check("a_log", a_log, f32, (H,))
+    _check("dt_bias", dt_bias, f32, (H * DK,))
+    _check("err", err, i32, allow_none=True)
+    a = _lib.KdaRecoverArgs()
+    a.batch, a.heads, a.tokens, a.num_slots = B, H, T, state.shape[0]
+    a.src_slots, a.dst_slots, a.accepted = (_ptr(src_slots), _ptr(dst_slots),
+                                            _ptr(accepted))
+    a.rec_u, a.rec_kg = _ptr(rec_u), _ptr(rec_kg)
+    a.a_log, a.dt_bias = _ptr(a_log), _ptr(dt_bias)
+    a.lower_bound = float(lower_bound)
+    a.state, a.err = _ptr(state), _ptr(err)
+    s = stream if stream is not None else torch.cuda.current_stream(state.device)
+    rc = _lib.call("kda_recover", a, s.cuda_stream)
+    if rc != _lib.KDA_SUCCESS:
+        raise _lib.KdaError(rc, _lib.strerror(rc))

@@ -16,13 +16,12 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(HERE, "libkda_gb300.so")
-SOURCES = [os.path.join(CSRC, "kda_step.cu")]
-HEADERS = [os.path.join(INCLUDE, "kda.h")]
+SOURCES = [os.path.join(CSRC, "kda_step.cu"), os.path.join(CSRC, "kda_recover.cu")]
+HEADERS = [os.path.join(INCLUDE, "kda.h"), os.path.join(CSRC, "kda_device.cuh")]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
-    "-O3", "-lineinfo", "-std=c++17",
-    "-shared", "-Xcompiler", "-fPIC",
+    "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
 ]
 
 
@@ -41,19 +40,37 @@ def is_stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library if missing or older than its sources."""
+    """Compile the library if missing or older than its sources.
+
+    Each translation unit compiles in its own nvcc process (in parallel), then
+    one nvcc call links the shared library."""
     if not force and not is_stale():
         return LIB_PATH
     with tempfile.TemporaryDirectory() as tmp:
+        procs = []
+        objs = []
+        for src in SOURCES:
+            obj = os.path.join(tmp, os.path.basename(src) + ".o")
+            cmd = [nvcc()] + NVCC_FLAGS + ["-I", INCLUDE, "-c", src, "-o", obj]
+            if verbose:
+                cmd.insert(1, "-Xptxas=-v")
+            procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                                stderr=subprocess.STDOUT, text=True)))
+            objs.append(obj)
+        logs = []
+        for src, pr in procs:
+            out, _ = pr.communicate()
+            logs.append(out)
+            if pr.returncode != 0:
+                raise RuntimeError(f"nvcc failed on {src}:\n{out}")
         out = os.path.join(tmp, "libkda_gb300.so")
-        cmd = [nvcc()] + NVCC_FLAGS + ["-I", INCLUDE, "-o", out] + SOURCES
-        if verbose:
-            cmd.insert(1, "-Xptxas=-v")
-        res = subprocess.run(cmd, capture_output=True, text=True)
+        link = [nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared",
+                "-o", out] + objs
+        res = subprocess.run(link, capture_output=True, text=True)
         if res.returncode != 0:
-            raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
+            raise RuntimeError("nvcc link failed:\n" + res.stdout + res.stderr)
         if verbose:
-            print(res.stdout + res.stderr)
+            print("".join(logs))
         os.replace(out, LIB_PATH)
     return LIB_PATH
 

@@ -29,7 +29,8 @@ KDA_DEVERR_SLOT = 1
 KDA_DEVERR_ACCEPTED = 2
 KDA_DEVERR_TIMEOUT = 4
 
-EXPORTED = ("kda_decode", "kda_verify", "kda_strerror", "kda_abi_version")
+EXPORTED = ("kda_decode", "kda_verify", "kda_recover", "kda_strerror",
+            "kda_abi_version")
 
 
 class KdaArgs(ctypes.Structure):
@@ -48,6 +49,17 @@ class KdaArgs(ctypes.Structure):
         ("lower_bound", ctypes.c_float), ("scale", ctypes.c_float),
         ("eps", ctypes.c_float),
         ("err", _P), ("dbg", _P),
+    ]
+
+
+class KdaRecoverArgs(ctypes.Structure):
+    """Mirror of ``struct kda_recover_args``."""
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("heads", ctypes.c_int32),
+        ("tokens", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+        ("src_slots", _P), ("dst_slots", _P), ("accepted", _P),
+        ("rec_u", _P), ("rec_kg", _P), ("a_log", _P), ("dt_bias", _P),
+        ("lower_bound", ctypes.c_float), ("state", _P), ("err", _P),
     ]
 
 
@@ -75,6 +87,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = [ctypes.POINTER(KdaArgs), ctypes.c_void_p]
         fn.restype = ctypes.c_int
+    lib.kda_recover.argtypes = [ctypes.POINTER(KdaRecoverArgs), ctypes.c_void_p]
+    lib.kda_recover.restype = ctypes.c_int
     lib.kda_strerror.argtypes = [ctypes.c_int]
     lib.kda_strerror.restype = ctypes.c_char_p
     lib.kda_abi_version.argtypes = []
@@ -88,7 +102,7 @@ def strerror(code: int) -> str:
     return load().kda_strerror(int(code)).decode()
 
 
-def call(entry: str, args: KdaArgs, stream_handle: int) -> int:
+def call(entry: str, args, stream_handle: int) -> int:
     """Raw call: returns the library's code without raising."""
     fn = getattr(load(), entry)
     return int(fn(ctypes.byref(args), ctypes.c_void_p(stream_handle or None)))

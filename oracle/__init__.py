@@ -61,6 +61,18 @@ class _Args(ctypes.Structure):
     ]
 
 
+class _RecoverArgs(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("heads", ctypes.c_int32),
+        ("tokens", ctypes.c_int32), ("dk", ctypes.c_int32),
+        ("num_slots", ctypes.c_int32),
+        ("src_slots", _P), ("dst_slots", _P), ("accepted", _P),
+        ("rec_u", _P), ("rec_kg", _P), ("a_log", _P), ("dt_bias", _P),
+        ("lower_bound", ctypes.c_float), ("state", _P), ("err", _P),
+        ("threads", ctypes.c_int32),
+    ]
+
+
 def _compile(out_path: str) -> None:
     os.makedirs(os.path.dirname(out_path), exist_ok=True)
     base = ["gcc", "-O2", "-std=gnu11", "-fPIC", "-ffp-contract=off",
@@ -106,6 +118,9 @@ def _load():
             fn = getattr(lib, f"kda_oracle_step_{sfx}")
             fn.argtypes = [ctypes.POINTER(_Args)]
             fn.restype = ctypes.c_int
+            rf = getattr(lib, f"kda_oracle_recover_{sfx}")
+            rf.argtypes = [ctypes.POINTER(_RecoverArgs)]
+            rf.restype = ctypes.c_int
             mt = getattr(lib, f"kda_oracle_max_threads_{sfx}")
             mt.restype = ctypes.c_int
         _lib = lib
@@ -209,3 +224,35 @@ def run(inputs: Dict[str, object], *, mode: str = "f32",
     if want_intermediates:
         res.update(inter=inter, pre=pre, o=o)
     return res
+
+
+def recover(*, state: np.ndarray, src_slots, dst_slots, accepted, rec_u: np.ndarray,
+            rec_kg: np.ndarray, a_log, dt_bias, lower_bound: float,
+            mode: str = "f32", in_place: bool = False, threads: int = 0):
+    """Record replay (see ``kda_oracle.c``): returns (state, err).
+
+    ``rec_u`` float32 [B, H, T, dk], ``rec_kg`` uint16 [B, H, T, 2*dk]."""
+    lib = _load()
+    st = _c(state, np.float32)
+    if not in_place:
+        st = st.copy()
+    B, H, T, D = rec_u.shape
+    keep = dict(src=np.ascontiguousarray(src_slots, dtype=np.int32),
+                dst=np.ascontiguousarray(dst_slots, dtype=np.int32),
+                acc=np.ascontiguousarray(accepted, dtype=np.int32),
+                ru=_c(rec_u, np.float32), rk=_c(rec_kg, np.uint16),
+                al=_c(np.asarray(a_log), np.float32),
+                dt=_c(np.asarray(dt_bias), np.float32))
+    err = np.zeros(1, dtype=np.int32)
+    a = _RecoverArgs()
+    a.batch, a.heads, a.tokens, a.dk, a.num_slots = B, H, T, D, st.shape[0]
+    a.src_slots, a.dst_slots, a.accepted = (_ptr(keep["src"]), _ptr(keep["dst"]),
+                                            _ptr(keep["acc"]))
+    a.rec_u, a.rec_kg = _ptr(keep["ru"]), _ptr(keep["rk"])
+    a.a_log, a.dt_bias = _ptr(keep["al"]), _ptr(keep["dt"])
+    a.lower_bound = float(lower_bound)
+    a.state, a.err, a.threads = _ptr(st), _ptr(err), int(threads)
+    rc = getattr(lib, f"kda_oracle_recover_{mode}")(ctypes.byref(a))
+    if rc != 0:
+        raise ValueError("oracle recover rejected its arguments")
+    return st, int(err[0])

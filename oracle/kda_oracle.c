@@ -421,6 +421,80 @@ int SUFFIXED(kda_oracle_step)(const kda_oracle_args *a) {
   return 0;
 }
 
+/* ---- record replay ---------------------------------------------------------
+ * The page's record mode ("RecoverSSM verify": checkpoint slot, records out)
+ * writes no state; it leaves per token the BF16 k before the L2 norm, the BF16
+ * raw gate and the FP32 u of every value row.  The replay the page refers to
+ * (RecoverSSM) is not shown; reading taken: for the first `accepted[r]` tokens
+ * of request r, starting from the checkpoint page, apply the recurrence's own
+ * state update with those records -- decay every key column by the decay of
+ * the recorded raw gate, then P += k_hat u (fused, k first) with k_hat the L2
+ * normalised recorded k -- and write the result to dst_slots[r].  This
+ * reproduces the state a non-record step writes after token accepted-1. */
+typedef struct {
+  int32_t batch, heads, tokens, dk, num_slots;
+  const int32_t *src_slots, *dst_slots, *accepted;
+  const float *rec_u;       /* [batch, heads, tokens, dk] */
+  const uint16_t *rec_kg;   /* bf16 [batch, heads, tokens, 2*dk] */
+  const float *a_log, *dt_bias;
+  float lower_bound;
+  float *state;             /* [num_slots, heads, dk, dk] in/out */
+  int32_t *err;
+  int32_t threads;
+} kda_oracle_recover_args;
+
+static int recover_item(const kda_oracle_recover_args *a, int r, int h) {
+  const int T = a->tokens, D = a->dk, H = a->heads;
+  const int src = a->src_slots[r], dst = a->dst_slots[r], acc = a->accepted[r];
+  if (src <= 0 || dst <= 0) return 0; /* padding: nothing written */
+  if (src >= a->num_slots || dst >= a->num_slots) return ORACLE_ERR_SLOT;
+  if (acc < 0 || acc > T) return ORACLE_ERR_ACCEPTED;
+  real *P = malloc(sizeof(real) * D * D), *kh = malloc(sizeof(real) * D);
+  real *dec = malloc(sizeof(real) * D);
+  const float *page = a->state + ((long)src * H + h) * (long)D * D;
+  for (long e = 0; e < (long)D * D; ++e) P[e] = (real)page[e];
+  const long item = (long)r * H + h;
+  for (int t = 0; t < acc; ++t) {
+    const uint16_t *kg = a->rec_kg + (item * T + t) * 2 * D;
+    const float *u = a->rec_u + (item * T + t) * D;
+    real sk = 0;
+    for (int c = 0; c < D; ++c) {
+      real kc = bf16_to_real(kg[c]);
+      real pk = kc * kc;
+      sk = sk + pk;
+    }
+    real fk = (real)1 / R_SQRT(sk + (real)1.0e-6);
+    for (int c = 0; c < D; ++c) kh[c] = bf16_to_real(kg[c]) * fk;
+    for (int f = 0; f < D; ++f)
+      dec[f] = decay_of((real)a->a_log[h], bf16_to_real(kg[D + f]),
+                        (real)a->dt_bias[(long)h * D + f], (real)a->lower_bound);
+    for (int i = 0; i < D; ++i)
+      for (int j = 0; j < D; ++j) P[i * D + j] = P[i * D + j] * dec[j];
+    for (int i = 0; i < D; ++i)
+      for (int j = 0; j < D; ++j) P[i * D + j] = R_FMA(kh[j], (real)u[i], P[i * D + j]);
+  }
+  float *out = a->state + ((long)dst * H + h) * (long)D * D;
+  for (long e = 0; e < (long)D * D; ++e) out[e] = (float)P[e];
+  free(P); free(kh); free(dec);
+  return 0;
+}
+
+/* Replays every item; src and dst pages of different requests must be
+ * distinct, and an item's dst may equal its src. */
+int SUFFIXED(kda_oracle_recover)(const kda_oracle_recover_args *a) {
+  if (a->tokens < 1 || a->tokens > 8) return -1;
+  const long n = (long)a->batch * a->heads;
+  int flags = 0;
+#ifdef _OPENMP
+  int nt = a->threads > 0 ? a->threads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nt) reduction(| : flags)
+#endif
+  for (long e = 0; e < n; ++e)
+    flags |= recover_item(a, (int)(e / a->heads), (int)(e % a->heads));
+  if (a->err) *a->err |= flags;
+  return 0;
+}
+
 /* Threads an OpenMP build will use by default (1 without OpenMP). */
 int SUFFIXED(kda_oracle_max_threads)(void) {
 #ifdef _OPENMP

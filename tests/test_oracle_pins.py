@@ -516,3 +516,64 @@ def test_static_argument_validation():
     for bad in (dict(tokens=0), dict(tokens=9), dict(gate_mode=2), dict(record=1)):
         with pytest.raises(ValueError):
             oracle.run(dict(o, **bad), mode="f32")
+
+
+# ------------------------------------------------------------ record replay
+
+@pytest.mark.parametrize("tokens", [2, 5])
+def test_record_replay_reproduces_per_token_states(tokens):
+    """Record verify + replay of a accepted tokens == the state a non-record
+    verify writes after token a-1, bit for bit (same FP32 operations)."""
+    T = tokens
+    w = tiny(dk=8, rank=16, tokens=T, slot_layout="verify", conv_width=T + 2,
+             num_slots=3 * T + 4, batch=3, heads=2, gate_mode=1, has_bias=True)
+    _, o = prepare(w)
+    B, H = w.batch, w.heads
+    # non-record verify: per-token states in slots[r, t]
+    ver = oracle.run(o, mode="f32")
+    # record verify of the same step: checkpoint slot = slots[r, accepted-1]
+    orec = dict(o, record=1)
+    rec = oracle.run(orec, mode="f32")
+    assert np.array_equal(rec["state"], o["state"])
+    for a in range(0, T + 1):
+        src = np.array([o["slots"][r, int(o["accepted"][r]) - 1] for r in range(B)],
+                       np.int32)
+        used = set(int(x) for x in o["slots"].ravel())
+        free = [x for x in range(1, w.num_slots) if x not in used]
+        dst = np.array(free[:B], np.int32)
+        st, err = oracle.recover(state=o["state"], src_slots=src, dst_slots=dst,
+                                 accepted=np.full(B, a, np.int32),
+                                 rec_u=rec["rec_u"], rec_kg=rec["rec_kg"],
+                                 a_log=o["a_log"], dt_bias=o["dt_bias"],
+                                 lower_bound=o["lower_bound"])
+        assert err == 0
+        for r in range(B):
+            if src[r] <= 0:
+                continue
+            for h in range(H):
+                want = (o["state"][src[r], h] if a == 0 else
+                        ver["state"][int(o["slots"][r, a - 1]), h])
+                assert np.array_equal(st[dst[r], h].view(np.uint32),
+                                      want.view(np.uint32)), (a, r, h)
+
+
+def test_record_replay_padding_and_errors():
+    T = 3
+    w = tiny(dk=8, rank=16, tokens=T, slot_layout="verify", conv_width=T + 2,
+             num_slots=12, batch=3, heads=2)
+    _, o = prepare(w)
+    rec = oracle.run(dict(o, record=1), mode="f32")
+    before = o["state"].copy()
+    st, err = oracle.recover(state=before, src_slots=[0, 2, 99], dst_slots=[5, 0, 6],
+                             accepted=[1, 2, 1], rec_u=rec["rec_u"],
+                             rec_kg=rec["rec_kg"], a_log=o["a_log"],
+                             dt_bias=o["dt_bias"], lower_bound=o["lower_bound"])
+    assert err == oracle.ERR_SLOT
+    assert np.array_equal(st, before)          # padding rows and the error row write nothing
+    st, err = oracle.recover(state=before, src_slots=[1, 2, 3], dst_slots=[4, 5, 6],
+                             accepted=[1, 9, 0], rec_u=rec["rec_u"],
+                             rec_kg=rec["rec_kg"], a_log=o["a_log"],
+                             dt_bias=o["dt_bias"], lower_bound=o["lower_bound"])
+    assert err == oracle.ERR_ACCEPTED
+    assert np.array_equal(st[6], before[3])     # accepted 0 copies the checkpoint
+    assert np.array_equal(st[5], before[5])     # the bad row wrote nothing
