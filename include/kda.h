@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 1
+#define KDA_ABI_VERSION 2
 #define KDA_DK 128
 #define KDA_MAX_TOKENS 8
 
@@ -67,7 +67,8 @@ enum {
   KDA_ERR_SHAPE = 8,          /* negative sizes, num_slots < 1, slot_cols <    */
                               /* tokens, or an item count beyond 2^31-1        */
   KDA_ERR_DEVICE = 9,         /* no usable device, or not an sm_103 device     */
-  KDA_ERR_LAUNCH = 10         /* the kernel launch failed (CUDA error)         */
+  KDA_ERR_LAUNCH = 10,        /* the kernel launch failed (CUDA error)         */
+  KDA_ERR_PATH = 11           /* path outside 0..2                             */
 };
 
 /* Device-side error flags, OR-ed into *err when err != NULL.  An item that
@@ -125,6 +126,11 @@ typedef struct kda_args {
   void *dbg;                /* optional bf16 [B, H, T, 4, 128]: q, k, v      */
                             /* (after SiLU, before the norm) and raw_g, as   */
                             /* this call rounded them; for parity checks     */
+  int32_t path;             /* kernel: 0 = automatic; 1 = persistent, one    */
+                            /* CTA per SM walking a range of items (for many */
+                            /* items); 2 = one item per cluster of 4 CTAs,   */
+                            /* each owning 32 value rows (for few items;     */
+                            /* ignores use_pdl).  Both give the same bits.   */
 } kda_args;
 
 /* One decode step (tokens == 1) on `stream` (a cudaStream_t; NULL = the

@@ -55,7 +55,8 @@ class KdaStep:
                  lower_bound: float, scale: float, eps: float,
                  tokens: int = 1, accepted=None, conv_bias=None,
                  gate_mode: int = 0, record: bool = False, rec_u=None,
-                 rec_kg=None, err=None, dbg=None, use_pdl: bool = False):
+                 rec_kg=None, err=None, dbg=None, use_pdl: bool = False,
+                 path: int = 0):
         bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
         T = int(tokens)
         if not 1 <= T <= 8:
@@ -119,6 +120,7 @@ class KdaStep:
         a.rec_u, a.rec_kg = _ptr(rec_u), _ptr(rec_kg)
         a.lower_bound, a.scale, a.eps = float(lower_bound), float(scale), float(eps)
         a.err, a.dbg = _ptr(err), _ptr(dbg)
+        a.path = int(path)
         self.args = a
         self.entry = "kda_decode" if T == 1 else "kda_verify"
         self.device = dev
@@ -155,7 +157,7 @@ INPUT_KEYS = ("x", "conv_weight", "conv_bias", "conv_state", "f_a", "f_b", "beta
 
 def step_from_inputs(dev_inputs: Dict[str, object], output: torch.Tensor, *,
                      rec_u=None, rec_kg=None, err=None, dbg=None,
-                     use_pdl: bool = False) -> KdaStep:
+                     use_pdl: bool = False, path: int = 0) -> KdaStep:
     """A ``KdaStep`` from a device copy of a seeded workload's input dict."""
     d = dev_inputs
     T = int(d["tokens"])
@@ -168,7 +170,7 @@ def step_from_inputs(dev_inputs: Dict[str, object], output: torch.Tensor, *,
         accepted=d.get("accepted") if T > 1 else None,
         conv_bias=d.get("conv_bias") if d.get("has_bias") else None,
         gate_mode=int(d["gate_mode"]), record=bool(d["record"]), rec_u=rec_u,
-        rec_kg=rec_kg, err=err, dbg=dbg, use_pdl=use_pdl)
+        rec_kg=rec_kg, err=err, dbg=dbg, use_pdl=use_pdl, path=path)
 
 
 def kda_recover(*, state, src_slots, dst_slots, accepted, rec_u, rec_kg, a_log,

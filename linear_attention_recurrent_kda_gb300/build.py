@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(HERE, "libkda_gb300.so")
-SOURCES = [os.path.join(CSRC, "kda_step.cu"), os.path.join(CSRC, "kda_recover.cu")]
+SOURCES = [os.path.join(CSRC, n) for n in ("kda_step.cu", "kda_split.cu",
+                                            "kda_recover.cu")]
 HEADERS = [os.path.join(INCLUDE, "kda.h"), os.path.join(CSRC, "kda_device.cuh")]
 
 NVCC_FLAGS = [

@@ -50,6 +50,9 @@
 
 namespace kda {
 
+// The cluster-split kernel (kda_split.cu) for few items.
+int launch_split(const kda_args *a, cudaStream_t stream);
+
 constexpr int kDk = 128;                          // dk = dv = gate rank
 constexpr int kRecThreads = 256;                  // warpgroups 0-1
 constexpr int kFrontThreads = 128;                // warpgroup 2
@@ -959,6 +962,7 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
   if (verify ? T == 1 : T != 1) return KDA_ERR_TOKENS;
   if (a->gate_mode != 0 && a->gate_mode != 1) return KDA_ERR_GATE_MODE;
   if (a->record && T == 1) return KDA_ERR_RECORD;
+  if (a->path < 0 || a->path > 2) return KDA_ERR_PATH;
   if (a->batch < 0 || a->heads < 0) return KDA_ERR_SHAPE;
   if (a->batch == 0 || a->heads == 0) return KDA_SUCCESS;
   if (a->num_slots < 1) return KDA_ERR_SHAPE;
@@ -1051,6 +1055,10 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
   prm.err = a->err;
   prm.dbg = static_cast<__nv_bfloat16 *>(a->dbg);
 
+  // Few items: one item per cluster of four CTAs (latency); many items: the
+  // persistent kernel (bandwidth).
+  const bool split = a->path == 2 || (a->path == 0 && 4 * prm.items <= 2 * di.sms);
+  if (split) return launch_split(a, stream);
   const int grid = prm.items < di.sms ? prm.items : di.sms;
   const int pdl = a->use_pdl ? 1 : 0;
   const bool rec = a->record != 0;
@@ -1098,6 +1106,7 @@ const char *kda_strerror(int code) {
     case KDA_ERR_SHAPE: return "invalid sizes";
     case KDA_ERR_DEVICE: return "no usable sm_103 device";
     case KDA_ERR_LAUNCH: return "kernel launch failed";
+    case KDA_ERR_PATH: return "path must be 0, 1 or 2";
     default: return "unknown error code";
   }
 }

@@ -25,6 +25,8 @@ KDA_ERR_ALIGNMENT = 7
 KDA_ERR_SHAPE = 8
 KDA_ERR_DEVICE = 9
 KDA_ERR_LAUNCH = 10
+KDA_ERR_PATH = 11
+KDA_PATH_AUTO, KDA_PATH_PERSISTENT, KDA_PATH_SPLIT = 0, 1, 2
 KDA_DEVERR_SLOT = 1
 KDA_DEVERR_ACCEPTED = 2
 KDA_DEVERR_TIMEOUT = 4
@@ -48,7 +50,7 @@ class KdaArgs(ctypes.Structure):
         ("rec_u", _P), ("rec_kg", _P),
         ("lower_bound", ctypes.c_float), ("scale", ctypes.c_float),
         ("eps", ctypes.c_float),
-        ("err", _P), ("dbg", _P),
+        ("err", _P), ("dbg", _P), ("path", ctypes.c_int32),
     ]
 
 

@@ -59,7 +59,7 @@ def to_device(inputs: Dict[str, object], device="cuda") -> Dict[str, object]:
 
 
 def run_gpu(inputs: Dict[str, object], *, dbg: bool = True, reps: int = 1,
-            stream: Optional[torch.cuda.Stream] = None) -> Dict[str, object]:
+            stream: Optional[torch.cuda.Stream] = None, path: int = 0) -> Dict[str, object]:
     """One step of the CUDA library on a device copy of ``inputs``."""
     d = to_device(inputs)
     B, H, T = d["batch"], d["heads"], d["tokens"]
@@ -72,7 +72,8 @@ def run_gpu(inputs: Dict[str, object], *, dbg: bool = True, reps: int = 1,
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     dbgt = (torch.zeros((B, H, T, 4, 128), dtype=torch.bfloat16, device=dev)
             if dbg else None)
-    step = step_from_inputs(d, out, rec_u=rec_u, rec_kg=rec_kg, err=err, dbg=dbgt)
+    step = step_from_inputs(d, out, rec_u=rec_u, rec_kg=rec_kg, err=err, dbg=dbgt,
+                            path=path)
     if stream is not None:
         stream.wait_stream(torch.cuda.current_stream())
     for _ in range(reps):

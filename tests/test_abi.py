@@ -33,8 +33,8 @@ def test_library_builds_and_exports_every_declared_symbol():
 
 
 def test_version_and_strerror():
-    assert kl.load().kda_abi_version() == 1
-    for code in range(0, 11):
+    assert kl.load().kda_abi_version() == 2
+    for code in range(0, 12):
         assert kl.strerror(code)
     assert "unknown" in kl.strerror(999)
 
