@@ -112,7 +112,7 @@ typedef struct kda_args {
   const int32_t *slots;     /* i32  [B] (decode) or [B, slot_cols] (verify)  */
   const int32_t *accepted;  /* i32  [B] (verify), ignored by decode          */
 
-  void *conv_state;         /* bf16 [num_slots, 3*dim, W]        in/out      */
+  void *conv_state;         /* bf16 (or f32, conv_f32) [num_slots, 3*dim, W] */
   float *state;             /* f32  [num_slots, H, 128, 128]     in/out      */
   void *output;             /* bf16 [B*T, dim]                   out         */
   float *rec_u;             /* f32  [B, H, T, 128]  record only, else NULL   */
@@ -131,6 +131,10 @@ typedef struct kda_args {
                             /* items); 2 = one item per cluster of 4 CTAs,   */
                             /* each owning 32 value rows (for few items;     */
                             /* ignores use_pdl).  Both give the same bits.   */
+  int32_t conv_f32;         /* conv_state holds FP32 instead of BF16: taps   */
+                            /* are read as stored and the new window is      */
+                            /* written as FP32 (the page's conv_type is the  */
+                            /* pool's element type)                          */
 } kda_args;
 
 /* One decode step (tokens == 1) on `stream` (a cudaStream_t; NULL = the

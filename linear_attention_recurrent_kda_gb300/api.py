@@ -72,7 +72,9 @@ class KdaStep:
         if state.dim() != 4 or tuple(state.shape[1:]) != (H, DK, DK):
             raise ValueError("state must be [num_slots, heads, 128, 128]")
         num_slots = state.shape[0]
-        _check("conv_state", conv_state, bf)
+        if not isinstance(conv_state, torch.Tensor) or conv_state.dtype not in (bf, f32):
+            raise TypeError("conv_state must be a bfloat16 or float32 tensor")
+        _check("conv_state", conv_state, conv_state.dtype)
         if conv_state.dim() != 3 or tuple(conv_state.shape[:2]) != (num_slots, 3 * dim):
             raise ValueError("conv_state must be [num_slots, 3*heads*128, width]")
         W = conv_state.shape[2]
@@ -121,6 +123,7 @@ class KdaStep:
         a.lower_bound, a.scale, a.eps = float(lower_bound), float(scale), float(eps)
         a.err, a.dbg = _ptr(err), _ptr(dbg)
         a.path = int(path)
+        a.conv_f32 = int(conv_state.dtype == f32)
         self.args = a
         self.entry = "kda_decode" if T == 1 else "kda_verify"
         self.device = dev

@@ -41,6 +41,7 @@ constexpr int kLive = 0, kPad = 1, kError = 2;
 
 struct Params {
   int32_t batch, heads, num_slots, conv_width, slot_cols, gate_mode, has_bias;
+  int32_t conv_f32;  // conv pool element: FP32 (1) or BF16 (0)
   const __nv_bfloat16 *x, *conv_weight, *conv_bias, *f_a, *f_b, *beta, *gate;
   const __nv_bfloat16 *norm_weight;
   const float *a_log, *dt_bias;
@@ -158,13 +159,8 @@ __global__ void __launch_bounds__(kThreads) kda_split_kernel(const __grid_consta
     const int64_t ch = pt * dim + h * kDk + c;
     const uint16_t *cw = reinterpret_cast<const uint16_t *>(p.conv_weight);
     const uint16_t *cb = reinterpret_cast<const uint16_t *>(p.conv_bias);
-    uint16_t *crow = reinterpret_cast<uint16_t *>(p.conv_state) +
-                     (static_cast<int64_t>(cs) * 3 * dim + ch) * p.conv_width;
-    const uint16_t tap0 = crow[off], tap1 = crow[off + 1], tap2 = crow[off + 2];
+    const int64_t rix = (static_cast<int64_t>(cs) * 3 * dim + ch) * p.conv_width;
     float win[3 + T];
-    win[0] = bf16_bits_to_float(tap0);
-    win[1] = bf16_bits_to_float(tap1);
-    win[2] = bf16_bits_to_float(tap2);
     uint16_t xb[T];
 #pragma unroll
     for (int t = 0; t < T; ++t) {
@@ -178,11 +174,28 @@ __global__ void __launch_bounds__(kThreads) kda_split_kernel(const __grid_consta
       wt[i] = bf16_bits_to_float(
           __ldg(cw + (static_cast<int64_t>(pt) * 4 + i) * dim + h * kDk + c));
     const float bias = p.has_bias ? bf16_bits_to_float(__ldg(cb + ch)) : 0.0f;
-    // New window [tap1, tap2, x_0 .. x_{T-1}] of this channel.
-    crow[0] = tap1;
-    crow[1] = tap2;
+    // Taps as the pool stores them (the page's conv_type); new window
+    // [tap1, tap2, x_0 .. x_{T-1}] of this channel.
+    if (p.conv_f32) {
+      float *crow = reinterpret_cast<float *>(p.conv_state) + rix;
+      win[0] = crow[off];
+      win[1] = crow[off + 1];
+      win[2] = crow[off + 2];
+      crow[0] = win[1];
+      crow[1] = win[2];
 #pragma unroll
-    for (int t = 0; t < T; ++t) crow[2 + t] = xb[t];
+      for (int t = 0; t < T; ++t) crow[2 + t] = win[3 + t];
+    } else {
+      uint16_t *crow = reinterpret_cast<uint16_t *>(p.conv_state) + rix;
+      const uint16_t tap0 = crow[off], tap1 = crow[off + 1], tap2 = crow[off + 2];
+      win[0] = bf16_bits_to_float(tap0);
+      win[1] = bf16_bits_to_float(tap1);
+      win[2] = bf16_bits_to_float(tap2);
+      crow[0] = tap1;
+      crow[1] = tap2;
+#pragma unroll
+      for (int t = 0; t < T; ++t) crow[2 + t] = xb[t];
+    }
 #pragma unroll
     for (int t = 0; t < T; ++t) {
       float acc = bias;
@@ -415,6 +428,7 @@ int launch_split(const kda_args *a, cudaStream_t stream) {
   prm.slots = a->slots;
   prm.accepted = a->accepted;
   prm.conv_state = static_cast<__nv_bfloat16 *>(a->conv_state);
+  prm.conv_f32 = a->conv_f32 ? 1 : 0;
   prm.state = a->state;
   prm.output = static_cast<__nv_bfloat16 *>(a->output);
   prm.rec_u = a->rec_u;

@@ -84,6 +84,7 @@ struct __align__(16) ItemDesc {
 
 struct Params {
   int32_t batch, heads, num_slots, conv_width, slot_cols, gate_mode, has_bias;
+  int32_t conv_f32;  // conv pool element: FP32 (1) or BF16 (0)
   int32_t items, stages;
   uint32_t stage_bytes, conv_off, x_off, gate_off, fa_off;
   uint32_t bar_off, desc_off, slot_off, slot_bytes, scratch_off, rscratch_off;
@@ -183,7 +184,7 @@ __device__ __forceinline__ int resolve_item(const Params &p, int n, ItemDesc &d)
 
 template <int T>
 __device__ __forceinline__ uint32_t small_bytes(const Params &p) {
-  return 3u * 256u * p.conv_width + 3u * T * 256u + 2u * T * 256u;
+  return 3u * (p.conv_f32 ? 512u : 256u) * p.conv_width + 3u * T * 256u + 2u * T * 256u;
 }
 
 __device__ __forceinline__ void issue_page(const Params &p, uint8_t *stage, int n,
@@ -201,13 +202,15 @@ __device__ __forceinline__ void issue_small(const Params &p, uint8_t *stage, int
   const int h = n / p.batch;
   const int r = n - h * p.batch;
   const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
-  const uint32_t row_bytes = 256u * p.conv_width;  // 128 channels x W bf16
+  const uint32_t elem = p.conv_f32 ? 4u : 2u;
+  const uint32_t row_bytes = 128u * elem * p.conv_width;  // 128 channels x W
 #pragma unroll
   for (int part = 0; part < 3; ++part) {
-    const __nv_bfloat16 *src =
-        p.conv_state + (static_cast<int64_t>(d.conv_slot) * 3 * dim + part * dim +
-                        static_cast<int64_t>(h) * kDk) *
-                           p.conv_width;
+    const uint8_t *src =
+        reinterpret_cast<const uint8_t *>(p.conv_state) +
+        (static_cast<int64_t>(d.conv_slot) * 3 * dim + part * dim +
+         static_cast<int64_t>(h) * kDk) *
+            p.conv_width * elem;
     bulk_g2s(stage + p.conv_off + part * row_bytes, src, row_bytes, bar);
   }
 #pragma unroll
@@ -390,12 +393,10 @@ __device__ __forceinline__ void front_item(const Params &p, const uint8_t *st,
   // tap order) and SiLU"): this thread owns channel c of q, k and v.
 #pragma unroll
   for (int part = 0; part < 3; ++part) {
-    const uint16_t *row = conv_s + (part * kDk + c) * p.conv_width;
-    const uint16_t tap0 = row[off], tap1 = row[off + 1], tap2 = row[off + 2];
+    // Taps of this channel, as the pool stores them (the page's conv_type).
+    const int64_t rix = (static_cast<int64_t>(cs) * 3 * dim + part * dim + h * kDk + c) *
+                        p.conv_width;
     float win[3 + T];
-    win[0] = bf16_bits_to_float(tap0);
-    win[1] = bf16_bits_to_float(tap1);
-    win[2] = bf16_bits_to_float(tap2);
     uint16_t xb[T];
 #pragma unroll
     for (int t = 0; t < T; ++t) {
@@ -403,13 +404,28 @@ __device__ __forceinline__ void front_item(const Params &p, const uint8_t *st,
       win[3 + t] = bf16_bits_to_float(xb[t]);
     }
     // New window [tap1, tap2, x_0 .. x_{T-1}] of this channel.
-    uint16_t *crow = reinterpret_cast<uint16_t *>(p.conv_state) +
-                     (static_cast<int64_t>(cs) * 3 * dim + part * dim + h * kDk + c) *
-                         p.conv_width;
-    crow[0] = tap1;
-    crow[1] = tap2;
+    if (p.conv_f32) {
+      const float *row = reinterpret_cast<const float *>(conv_s) + (part * kDk + c) * p.conv_width;
+      win[0] = row[off];
+      win[1] = row[off + 1];
+      win[2] = row[off + 2];
+      float *crow = reinterpret_cast<float *>(p.conv_state) + rix;
+      crow[0] = win[1];
+      crow[1] = win[2];
 #pragma unroll
-    for (int t = 0; t < T; ++t) crow[2 + t] = xb[t];
+      for (int t = 0; t < T; ++t) crow[2 + t] = win[3 + t];
+    } else {
+      const uint16_t *row = conv_s + (part * kDk + c) * p.conv_width;
+      const uint16_t tap0 = row[off], tap1 = row[off + 1], tap2 = row[off + 2];
+      win[0] = bf16_bits_to_float(tap0);
+      win[1] = bf16_bits_to_float(tap1);
+      win[2] = bf16_bits_to_float(tap2);
+      uint16_t *crow = reinterpret_cast<uint16_t *>(p.conv_state) + rix;
+      crow[0] = tap1;
+      crow[1] = tap2;
+#pragma unroll
+      for (int t = 0; t < T; ++t) crow[2 + t] = xb[t];
+    }
 #pragma unroll
     for (int t = 0; t < T; ++t) {
       float acc = fc.bias[part];
@@ -881,9 +897,10 @@ static uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 // hand-off slots and the partial-sum scratch.  Decode uses two stages and as
 // many 16 KiB quarter buffers (up to 4) as fit; verify and record steps take
 // three stages when they fit, else two.
-static bool make_layout(int T, int W, bool record, int max_smem, Layout &L) {
+static bool make_layout(int T, int W, bool record, bool conv_f32, int max_smem,
+                        Layout &L) {
   L.conv_off = kPageBytes;
-  L.x_off = align_up(L.conv_off + 3u * 256u * W, 128);
+  L.x_off = align_up(L.conv_off + 3u * (conv_f32 ? 512u : 256u) * W, 128);
   L.gate_off = L.x_off + 3u * T * 256u;
   L.fa_off = L.gate_off + T * 256u;
   L.stage_bytes = align_up(L.fa_off + T * 256u, 128);
@@ -1006,7 +1023,7 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
     di.ok = true;
   }
   Layout L;
-  if (!make_layout(T, a->conv_width, a->record != 0, di.max_smem, L))
+  if (!make_layout(T, a->conv_width, a->record != 0, a->conv_f32 != 0, di.max_smem, L))
     return KDA_ERR_CONV_WIDTH;
 
   Params prm;
@@ -1045,6 +1062,7 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
   prm.slots = a->slots;
   prm.accepted = a->accepted;
   prm.conv_state = static_cast<__nv_bfloat16 *>(a->conv_state);
+  prm.conv_f32 = a->conv_f32 ? 1 : 0;
   prm.state = a->state;
   prm.output = static_cast<__nv_bfloat16 *>(a->output);
   prm.rec_u = a->rec_u;

@@ -11,7 +11,7 @@ variance, for every N(0, s)):
 
 ====================  ===================================================
 x                     N(0, 1) BF16 [B*T, 3*H*dk]   (q | k | v blocks)
-conv_state            N(0, 1) BF16 [num_slots, 3*H*dk, conv_width]
+conv_state            N(0, 1) BF16 (or FP32) [num_slots, 3*H*dk, conv_width]
 conv_weight           N(0, 0.5) BF16 [3, 4, H*dk]
 conv_bias             N(0, 0.5) BF16 [3*H*dk]      (has_bias only)
 f_a                   N(0, 1) BF16 [B*T, rank]
@@ -61,6 +61,7 @@ class Workload:
     seed: int = 1000
     lower_bound: float = -5.0
     eps: float = 1e-6
+    conv_dtype: str = "bf16"  # "bf16" | "f32": element type of the conv pool
 
     @property
     def dim(self) -> int:
@@ -123,7 +124,8 @@ def make_inputs(w: Workload) -> Dict[str, object]:
 
     out: Dict[str, object] = {}
     out["x"] = _bf16(randn(rows, 3 * dim))
-    out["conv_state"] = _bf16(randn(w.num_slots, 3 * dim, w.conv_width))
+    conv = randn(w.num_slots, 3 * dim, w.conv_width)
+    out["conv_state"] = conv if w.conv_dtype == "f32" else _bf16(conv)
     out["conv_weight"] = _bf16(randn(3, 4, dim, std=0.5))
     out["conv_bias"] = _bf16(randn(3 * dim, std=0.5)) if w.has_bias else None
     out["f_a"] = _bf16(randn(rows, R))

@@ -58,6 +58,7 @@ class _Args(ctypes.Structure):
         ("items", _P), ("n_items", ctypes.c_int32),
         ("inter_out", _P), ("pre_out", _P), ("inter_in", _P), ("o_out", _P),
         ("err", _P), ("threads", ctypes.c_int32),
+        ("conv_f32", ctypes.c_int32), ("conv_state_f32", _P),
     ]
 
 
@@ -185,7 +186,8 @@ def run(inputs: Dict[str, object], *, mode: str = "f32",
         "accepted": _c(inputs.get("accepted"), i32) if T > 1 else None,
     }
     state = _c(inputs["state"], f32)
-    conv_state = _c(inputs["conv_state"], u16)
+    conv_f32 = np.asarray(inputs["conv_state"]).dtype == np.float32
+    conv_state = _c(inputs["conv_state"], f32 if conv_f32 else u16)
     if not in_place:
         state = state.copy()
         conv_state = conv_state.copy()
@@ -204,7 +206,10 @@ def run(inputs: Dict[str, object], *, mode: str = "f32",
         setattr(a, k, st[k])
     for k, v in keep.items():
         setattr(a, k, _ptr(v))
-    a.conv_state, a.state, a.output = _ptr(conv_state), _ptr(state), _ptr(out)
+    a.conv_state = None if conv_f32 else _ptr(conv_state)
+    a.conv_f32 = int(conv_f32)
+    a.conv_state_f32 = _ptr(conv_state) if conv_f32 else None
+    a.state, a.output = _ptr(state), _ptr(out)
     a.rec_u, a.rec_kg = _ptr(rec_u), _ptr(rec_kg)
     a.lower_bound = float(inputs["lower_bound"])
     a.scale = float(inputs["scale"])

@@ -96,6 +96,11 @@ typedef struct {
   double *o_out;             /* [batch,heads,tokens,dk]: o before rounding   */
   int32_t *err;              /* OR of ORACLE_ERR_* over items                */
   int32_t threads;           /* OpenMP threads (<=0: library default)        */
+  /* FP32 conv state (the page's conv_type is the pool's own element type):
+   * when conv_f32 != 0, conv_state_f32 [num_slots, 3*dim, W] replaces
+   * conv_state; taps are read as stored and the window is written as FP32. */
+  int32_t conv_f32;
+  float *conv_state_f32;
 } kda_oracle_args;
 
 /* ---- BF16 <-> binary floating point -------------------------------------- */
@@ -223,7 +228,7 @@ static int run_item(const kda_oracle_args *a, int r, int h) {
   real *kn = malloc(sizeof(real) * T * D), *ob = malloc(sizeof(real) * T * D);
   real *P = malloc(sizeof(real) * D * D), *u = malloc(sizeof(real) * D);
   real beta_t[8];
-  uint16_t *old_taps = malloc(sizeof(uint16_t) * 3 * D * 3);
+  real *old_taps = malloc(sizeof(real) * 3 * D * 3);
   real *parts[3] = {q, k, v};
 
   /* Short causal depthwise convolution + SiLU (KdaWide.kernel, "The
@@ -234,11 +239,12 @@ static int run_item(const kda_oracle_args *a, int r, int h) {
   for (int p = 0; p < 3; ++p) {
     for (int c = 0; c < D; ++c) {
       const long ch = (long)p * dim + (long)h * D + c;
-      const uint16_t *row = a->conv_state + ((long)cs * 3 * dim + ch) * W;
+      const long rowix = ((long)cs * 3 * dim + ch) * W;
       real win[3 + 8];
       for (int i = 0; i < 3; ++i) {
-        old_taps[(p * D + c) * 3 + i] = row[off + i];
-        win[i] = bf16_to_real(row[off + i]);
+        win[i] = a->conv_f32 ? (real)a->conv_state_f32[rowix + off + i]
+                             : bf16_to_real(a->conv_state[rowix + off + i]);
+        old_taps[(p * D + c) * 3 + i] = win[i];
       }
       for (int t = 0; t < T; ++t)
         win[3 + t] = bf16_to_real(a->x[((long)r * T + t) * 3 * dim + ch]);
@@ -386,10 +392,19 @@ static int run_item(const kda_oracle_args *a, int r, int h) {
   for (int p = 0; p < 3; ++p)
     for (int c = 0; c < D; ++c) {
       const long ch = (long)p * dim + (long)h * D + c;
-      uint16_t *row = a->conv_state + ((long)cs * 3 * dim + ch) * W;
-      row[0] = old_taps[(p * D + c) * 3 + 1];
-      row[1] = old_taps[(p * D + c) * 3 + 2];
-      for (int t = 0; t < T; ++t) row[2 + t] = a->x[((long)r * T + t) * 3 * dim + ch];
+      const long rowix = ((long)cs * 3 * dim + ch) * W;
+      if (a->conv_f32) {
+        float *row = a->conv_state_f32 + rowix;
+        row[0] = (float)old_taps[(p * D + c) * 3 + 1];
+        row[1] = (float)old_taps[(p * D + c) * 3 + 2];
+        for (int t = 0; t < T; ++t)
+          row[2 + t] = (float)bf16_to_real(a->x[((long)r * T + t) * 3 * dim + ch]);
+      } else {
+        uint16_t *row = a->conv_state + rowix;
+        row[0] = real_to_bf16(old_taps[(p * D + c) * 3 + 1]);
+        row[1] = real_to_bf16(old_taps[(p * D + c) * 3 + 2]);
+        for (int t = 0; t < T; ++t) row[2 + t] = a->x[((long)r * T + t) * 3 * dim + ch];
+      }
     }
 
   free(q); free(k); free(v); free(graw); free(dec); free(qn); free(kn);

@@ -577,3 +577,51 @@ def test_record_replay_padding_and_errors():
     assert err == oracle.ERR_ACCEPTED
     assert np.array_equal(st[6], before[3])     # accepted 0 copies the checkpoint
     assert np.array_equal(st[5], before[5])     # the bad row wrote nothing
+
+
+# ------------------------------------------------------------ FP32 conv state
+
+def test_fp32_conv_state_holding_bf16_values_matches_bf16_pool():
+    T = 3
+    w = tiny(dk=8, rank=16, tokens=T, slot_layout="verify", conv_width=T + 3,
+             num_slots=12, has_bias=True)
+    _, o = prepare(w)
+    o32 = dict(o, conv_state=f64(o["conv_state"]).astype(np.float32))
+    a = oracle.run(o, mode="f32")
+    b = oracle.run(o32, mode="f32")
+    for k in ("output", "state"):
+        assert np.array_equal(a[k], b[k])
+    assert np.array_equal(f64(a["conv_state"]).astype(np.float32), b["conv_state"])
+
+
+def test_fp32_conv_state_uses_unrounded_taps():
+    T = 2
+    w = tiny(tokens=T, slot_layout="verify", conv_width=T + 2, num_slots=10,
+             conv_dtype="f32")
+    _, o = prepare(w)
+    assert o["conv_state"].dtype == np.float32
+    res = oracle.run(o, mode="f64", want_intermediates=True)
+    D, H = w.dk, w.heads
+    for r in range(w.batch):
+        sel = resolve(o, r)
+        if sel is None:
+            continue
+        s, cs, off = sel
+        for h in range(H):
+            for part in range(3):
+                for c in range(D):
+                    ch = part * H * D + h * D + c
+                    taps = o["conv_state"][cs, ch, off:off + 3].astype(np.float64)
+                    xs = f64(o["x"][r * T:(r + 1) * T, ch])
+                    wt = f64(o["conv_weight"][part, :, h * D + c])
+                    y = tb.silu(tb.causal_conv4(taps, xs, wt))
+                    np.testing.assert_allclose(res["pre"][r, h, :, part, c], y,
+                                               rtol=1e-13, atol=1e-15)
+            # window written as FP32: [tap1, tap2, x_0 .. x_{T-1}]
+            ch = np.arange(3 * H * D).reshape(3, H, D)[:, h, :].ravel()
+            new = res["conv_state"][cs][ch, :T + 2]
+            old = o["conv_state"][cs][ch]
+            assert np.array_equal(new[:, 0], old[:, off + 1])
+            assert np.array_equal(new[:, 1], old[:, off + 2])
+            xcols = f64(o["x"][r * T:(r + 1) * T][:, ch]).T.astype(np.float32)
+            assert np.array_equal(new[:, 2:], xcols)
