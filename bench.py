@@ -215,6 +215,59 @@ def cpu_baseline(workload, budget_s=12.0):
                       f"repeated) in {dt:.1f} s"}
 
 
+def run_recover(args):
+    """Times kda_recover on a record-mode workload (single GPU): one record
+    verify produces the records, then each step replays accepted ~ U{1..T}
+    tokens of every item in place (checkpoint page -> same slot)."""
+    import torch
+    from linear_attention_recurrent_kda_gb300.api import kda_recover, step_from_inputs
+    from linear_attention_recurrent_kda_gb300.workloads import WORKLOADS, make_inputs
+    name = args.workload if WORKLOADS[args.workload].record else "verify_q8_record_b64_h64"
+    w = WORKLOADS[name]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    host = make_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    B, H, T = w.batch, w.heads, w.tokens
+    out = torch.empty((B * T, H * 128), dtype=torch.bfloat16, device=dev)
+    ru = torch.empty((B, H, T, 128), dtype=torch.float32, device=dev)
+    rk = torch.empty((B, H, T, 256), dtype=torch.bfloat16, device=dev)
+    step_from_inputs(d, out, rec_u=ru, rec_kg=rk)()
+    src = torch.tensor([int(host["slots"][r, int(host["accepted"][r]) - 1])
+                        for r in range(B)], dtype=torch.int32, device=dev)
+    acc = torch.randint(1, T + 1, (B,), generator=torch.Generator().manual_seed(3),
+                        dtype=torch.int32).to(dev)
+
+    def call():
+        kda_recover(state=d["state"], src_slots=src, dst_slots=src, accepted=acc,
+                    rec_u=ru, rec_kg=rk, a_log=d["a_log"], dt_bias=d["dt_bias"],
+                    lower_bound=w.lower_bound)
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    live = int((src > 0).sum()) * H
+    acc_live = int(acc[src > 0].sum()) * H
+    nbytes = live * 2 * 128 * 128 * 4 + acc_live * (128 * 4 + 256 * 2) + B * 12
+    peak, kind = measured_peak()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "KDA record replay (req,head) items/s", "op": "recover",
+        "value": live / (ms * 1e-3), "unit": "items/s", "ms_per_step": ms,
+        "steps": args.steps, "config": {"workload": name, "items_live": live,
+                                        "replayed_tokens": acc_live},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "peak_source": f"{kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": nbytes}}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -223,6 +276,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="decode_b256_h32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="step", choices=["step", "recover"],
+                    help="step: the decode/verify step (default); recover: the "
+                         "record replay after a record-mode verify")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -233,6 +289,9 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, workload)), flush=True)
+        return
+    if args.op == "recover":
+        run_recover(args)
         return
 
     import torch
