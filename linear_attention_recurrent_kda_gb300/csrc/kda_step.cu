@@ -612,11 +612,16 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
     const int stage = k % S;
     const uint32_t round = static_cast<uint32_t>(k / S);
     bool ok = mbar_wait(&ctl->full[stage], round & 1u, &ctl->abort);
+    // Every thread reads the item's status BEFORE the barrier: thread 0 frees
+    // a non-live item's stage right after it, and the producer then rewrites
+    // the descriptor; a read after that could see the next item's status and
+    // split the recurrence warps between two barrier sequences.
+    const bool live = ok && desc[stage].status == kLive;
     if (rec_sync_or(!ok)) {
       if (T > 1 && !RECORD && tid == 0) bulk_wait_all();
       return;
     }
-    if (desc[stage].status != kLive) {
+    if (!live) {
       if (tid == 0) mbar_arrive(&ctl->empty[stage]);
       continue;
     }
