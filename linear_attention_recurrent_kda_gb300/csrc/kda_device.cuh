@@ -300,6 +300,17 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// warp_sum of N independent values, reduced level by level so that the N
+// shuffle chains overlap; each value sees the same additions as warp_sum.
+template <int N>
+__device__ __forceinline__ void warp_sum_n(float (&v)[N]) {
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1)
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      v[i] = __fadd_rn(v[i], __shfl_xor_sync(0xffffffffu, v[i], s));
+}
+
 // Sum over the 8 lanes of a row group of four partial sums (one per value row
 // m = 0..3); returns the total of row (lane >> 1) & 3.
 __device__ __forceinline__ float reduce_scatter8(const float (&x)[4], int l) {

@@ -19,13 +19,14 @@
 //                  items ahead;
 //       front      (warpgroup 2): item j's conv + SiLU, gate projection on
 //                  tensor cores (mma.sync m16n8k16 BF16, FP32 accumulate),
-//                  decay, beta, L2 norms, sigmoid(gate) -> a double-buffered
-//                  hand-off slot;
+//                  decay, beta, L2 norms -> a double-buffered hand-off slot;
+//                  before that, the gated RMSNorm of the item the recurrence
+//                  last finished in that slot (o and gate are there);
 //       recurrence (warpgroups 0-1): item j-1's delta rule with the page in
 //                  registers: thread (g = tid/8, l = tid%8) holds keys
 //                  {32c + 4l + e} of value rows g, g+32, g+64, g+96 (64
 //                  floats), packed FP32 (f32x2) multiplies/FMAs, row sums by an
-//                  8-lane reduce-scatter; then the gated RMSNorm epilogue.
+//                  8-lane reduce-scatter; o goes back into the slot.
 //                  Updated pages leave shared memory through TMA bulk stores,
 //                  so no per-thread global stores queue in L1TEX:
 //                  decode: the page goes, one 16 KiB quarter (32 rows) at a
@@ -35,7 +36,10 @@
 //                  is refilled as soon as the page is in registers;
 //                  verify: after each written token the page goes back into
 //                  its stage buffer and the recurrence leader bulk-stores it;
-//                  the stage is released after the last store has read it.
+//                  the stage is released once the last store has read it.
+//                  Verify and record steps
+//                  also send the new conv windows back from the staged rows
+//                  with bulk stores (decode's 3-element windows go direct).
 //     The time per item is max(front, recurrence), not their sum.
 //   * setmaxnreg moves registers from the producer warpgroup (40 a thread) to
 //     the recurrence (160) and front (144) warpgroups; launch gives 128.
@@ -371,9 +375,13 @@ __device__ __forceinline__ void load_front_const(const Params &p, int h, int c,
 }
 
 // Front of one live item: conv + SiLU + BF16, gate projection + decay, beta,
-// L2 norms, written to slot `sv`.  Releases the stage once its reads are done.
+// L2 norms, written to slot `sv`.  Conv windows: decode stores each channel's
+// new window (T + 2 elements) directly and releases the stage as soon as its
+// reads are done; verify and record steps (longer windows) write them over
+// the staged conv rows, which leave through three TMA bulk stores issued by
+// channel 0, and release the stage once those stores have read it.
 template <int T, bool RECORD>
-__device__ __forceinline__ void front_item(const Params &p, const uint8_t *st,
+__device__ __forceinline__ void front_item(const Params &p, uint8_t *st,
                                            const ItemDesc &dsc, int n,
                                            const SlotView<T> &sv, float *ssum,
                                            const FrontConst &fc, int c,
@@ -384,66 +392,90 @@ __device__ __forceinline__ void front_item(const Params &p, const uint8_t *st,
   const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
   const int64_t item = static_cast<int64_t>(r) * p.heads + h;
   const int cs = dsc.conv_slot, off = dsc.offset;
-  const uint16_t *conv_s = reinterpret_cast<const uint16_t *>(st + p.conv_off);
+  uint16_t *conv_s = reinterpret_cast<uint16_t *>(st + p.conv_off);
   const uint16_t *x_s = reinterpret_cast<const uint16_t *>(st + p.x_off);
   const uint16_t *gate_s = reinterpret_cast<const uint16_t *>(st + p.gate_off);
   const uint16_t *fa_s = reinterpret_cast<const uint16_t *>(st + p.fa_off);
 
   // --- convolution + SiLU + BF16 (KdaWide.kernel, "The convolution (stock
-  // tap order) and SiLU"): this thread owns channel c of q, k and v.
+  // tap order) and SiLU"): this thread owns channel c of q, k and v.  Loads,
+  // window writes, arithmetic and stores are separate phases so that the
+  // independent per-(part, token) chains overlap.
+  uint16_t xb[3][T];
+  float tap[3][3];
+#pragma unroll
+  for (int part = 0; part < 3; ++part)
+#pragma unroll
+    for (int t = 0; t < T; ++t) xb[part][t] = x_s[(t * 3 + part) * kDk + c];
+  // Taps of this channel, as the pool stores them (the page's conv_type), and
+  // its new window [tap1, tap2, x_0 .. x_{T-1}]: to the pool (decode) or over
+  // its staged row (columns past T + 1 keep their loaded values).
 #pragma unroll
   for (int part = 0; part < 3; ++part) {
-    // Taps of this channel, as the pool stores them (the page's conv_type).
     const int64_t rix = (static_cast<int64_t>(cs) * 3 * dim + part * dim + h * kDk + c) *
                         p.conv_width;
-    float win[3 + T];
-    uint16_t xb[T];
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      xb[t] = x_s[(t * 3 + part) * kDk + c];
-      win[3 + t] = bf16_bits_to_float(xb[t]);
-    }
-    // New window [tap1, tap2, x_0 .. x_{T-1}] of this channel.
     if (p.conv_f32) {
-      const float *row = reinterpret_cast<const float *>(conv_s) + (part * kDk + c) * p.conv_width;
-      win[0] = row[off];
-      win[1] = row[off + 1];
-      win[2] = row[off + 2];
-      float *crow = reinterpret_cast<float *>(p.conv_state) + rix;
-      crow[0] = win[1];
-      crow[1] = win[2];
+      float *row = reinterpret_cast<float *>(conv_s) + (part * kDk + c) * p.conv_width;
 #pragma unroll
-      for (int t = 0; t < T; ++t) crow[2 + t] = win[3 + t];
+      for (int i = 0; i < 3; ++i) tap[part][i] = row[off + i];
+      float *dst = (T == 1) ? reinterpret_cast<float *>(p.conv_state) + rix : row;
+      dst[0] = tap[part][1];
+      dst[1] = tap[part][2];
+#pragma unroll
+      for (int t = 0; t < T; ++t) dst[2 + t] = bf16_bits_to_float(xb[part][t]);
     } else {
-      const uint16_t *row = conv_s + (part * kDk + c) * p.conv_width;
-      const uint16_t tap0 = row[off], tap1 = row[off + 1], tap2 = row[off + 2];
-      win[0] = bf16_bits_to_float(tap0);
-      win[1] = bf16_bits_to_float(tap1);
-      win[2] = bf16_bits_to_float(tap2);
-      uint16_t *crow = reinterpret_cast<uint16_t *>(p.conv_state) + rix;
-      crow[0] = tap1;
-      crow[1] = tap2;
+      uint16_t *row = conv_s + (part * kDk + c) * p.conv_width;
+      uint16_t tb[3];
 #pragma unroll
-      for (int t = 0; t < T; ++t) crow[2 + t] = xb[t];
+      for (int i = 0; i < 3; ++i) {
+        tb[i] = row[off + i];
+        tap[part][i] = bf16_bits_to_float(tb[i]);
+      }
+      uint16_t *dst = (T == 1) ? reinterpret_cast<uint16_t *>(p.conv_state) + rix : row;
+      dst[0] = tb[1];
+      dst[1] = tb[2];
+#pragma unroll
+      for (int t = 0; t < T; ++t) dst[2 + t] = xb[part][t];
     }
+  }
+  float y[3][T];
+#pragma unroll
+  for (int part = 0; part < 3; ++part) {
 #pragma unroll
     for (int t = 0; t < T; ++t) {
       float acc = fc.bias[part];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc = __fmaf_rn(win[t + i], fc.wt[part][i], acc);
-      const float y = bf16_round(silu_approx(acc));
-      if (part == 0) sv.q[t * kDk + c] = y;
-      else if (part == 1) sv.k[t * kDk + c] = y;
-      else sv.v[t * kDk + c] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-      if (p.dbg) p.dbg[((item * T + t) * 4 + part) * kDk + c] = __float2bfloat16_rn(y);
-      if (RECORD && part == 1)
-        p.rec_kg[(item * T + t) * 2 * kDk + c] = __float2bfloat16_rn(y);
-      if (part < 2) {
-        const float sq = warp_sum(__fmul_rn(y, y));
-        if (lane == 0) ssum[(t * 2 + part) * 4 + fw] = sq;
+      for (int i = 0; i < 4; ++i) {
+        const float w = (t + i < 3) ? tap[part][t + i] : bf16_bits_to_float(xb[part][t + i - 3]);
+        acc = __fmaf_rn(w, fc.wt[part][i], acc);
       }
+      y[part][t] = bf16_round(silu_approx(acc));
     }
   }
+  float sq[2 * T];
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    sv.q[t * kDk + c] = y[0][t];
+    sv.k[t * kDk + c] = y[1][t];
+    sv.v[t * kDk + c] = __bfloat16_as_ushort(__float2bfloat16_rn(y[2][t]));
+    if (RECORD) p.rec_kg[(item * T + t) * 2 * kDk + c] = __float2bfloat16_rn(y[1][t]);
+    sq[2 * t] = __fmul_rn(y[0][t], y[0][t]);
+    sq[2 * t + 1] = __fmul_rn(y[1][t], y[1][t]);
+  }
+  if (p.dbg) {
+#pragma unroll
+    for (int part = 0; part < 3; ++part)
+#pragma unroll
+      for (int t = 0; t < T; ++t)
+        p.dbg[((item * T + t) * 4 + part) * kDk + c] = __float2bfloat16_rn(y[part][t]);
+  }
+  warp_sum_n(sq);
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < 2 * T; ++i) ssum[i * 4 + fw] = sq[i];
+  }
+  // The rewritten conv rows are read next by the async proxy (bulk stores).
+  if (T > 1) fence_proxy_async_smem();
 #pragma unroll
   for (int t = 0; t < T; ++t) sv.gate[t * kDk + c] = gate_s[t * kDk + c];
   if (c < T) {
@@ -470,8 +502,8 @@ __device__ __forceinline__ void front_item(const Params &p, const uint8_t *st,
         fb1[kc] = 0u;
       }
     }
-    // All reads of the stage (and its descriptor) by this thread are done.
-    mbar_arrive(empty_bar);
+    // Decode: all reads of the stage (and its descriptor) are done.
+    if (T == 1) mbar_arrive(empty_bar);
     // gate_mode 0: one chain per tile, the two tiles interleaved; gate_mode
     // 1: four chains of two MMAs per tile, 0 + (((c0 + c1) + c2) + c3).
     float gv[2][4];
@@ -526,6 +558,21 @@ __device__ __forceinline__ void front_item(const Params &p, const uint8_t *st,
     }
   }
   front_sync();
+  if (T > 1 && c == 0) {
+    // Every channel's new window is in the staged rows: store them back.
+    const uint32_t elem = p.conv_f32 ? 4u : 2u;
+    const uint32_t row_bytes = 128u * elem * p.conv_width;
+    const uint64_t pol = policy_evict_first();
+    const int64_t hd = static_cast<int64_t>(p.heads) * kDk;
+    const int64_t row0 = static_cast<int64_t>(dsc.conv_slot) * 3 * hd +
+                         static_cast<int64_t>(n / p.batch) * kDk;
+#pragma unroll
+    for (int part = 0; part < 3; ++part)
+      bulk_s2g(reinterpret_cast<uint8_t *>(p.conv_state) +
+                   (row0 + part * hd) * p.conv_width * elem,
+               st + p.conv_off + part * row_bytes, row_bytes, pol);
+    bulk_commit();
+  }
 
   // --- L2 norms ("Normalized q (with the 1/sqrt(K) scale) and k"), partial
   // sums combined as KdaWide.quad_sum does.
@@ -541,6 +588,51 @@ __device__ __forceinline__ void front_item(const Params &p, const uint8_t *st,
     sv.q[t * kDk + c] = __fmul_rn(__fmul_rn(sv.q[t * kDk + c], fq), p.scale);
     sv.k[t * kDk + c] = __fmul_rn(sv.k[t * kDk + c], fk);
   }
+  if (T > 1) {
+    // All reads of the stage (and its descriptor) are done; channel 0 also
+    // waits until its conv-row stores have read the stage.
+    if (c == 0) bulk_wait_read(0);
+    mbar_arrive(empty_bar);
+  }
+}
+
+// Gated RMSNorm ("Gated RMSNorm") of the item whose o the recurrence left in
+// slot `sv`: thread = channel c; the four warps' partial sums of a token are
+// combined as KdaWide.quad_sum does.  `osum` ([T][4]) is free on entry.
+template <int T>
+__device__ __forceinline__ void front_epilogue(const Params &p, const SlotView<T> &sv,
+                                               float *osum, float nw, int c) {
+  const int lane = c & 31, fw = c >> 5;
+  const int n = sv.meta[0];
+  const int h = n / p.batch;
+  const int r = n - h * p.batch;
+  const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
+  float ov[T], gv[T], tot[T];
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    ov[t] = bf16_bits_to_float(sv.o[t * kDk + c]);
+    gv[t] = bf16_bits_to_float(sv.gate[t * kDk + c]);
+    tot[t] = __fmul_rn(ov[t], ov[t]);
+  }
+  warp_sum_n(tot);
+  if (lane == 0) {
+#pragma unroll
+    for (int t = 0; t < T; ++t) osum[t * 4 + fw] = tot[t];
+  }
+  front_sync();
+  float y[T];
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    const float4 o4 = *reinterpret_cast<const float4 *>(osum + t * 4);
+    const float sumsq = __fadd_rn(__fadd_rn(o4.x, o4.z), __fadd_rn(o4.y, o4.w));
+    const float var = __fadd_rn(__fmul_rn(sumsq, 1.0f / 128.0f), p.eps);
+    const float rstd = rcp_approx(sqrt_approx(var));
+    y[t] = __fmul_rn(__fmul_rn(__fmul_rn(ov[t], rstd), nw), sigmoid_approx(gv[t]));
+  }
+#pragma unroll
+  for (int t = 0; t < T; ++t)
+    p.output[(static_cast<int64_t>(r) * T + t) * dim + h * kDk + c] =
+        __float2bfloat16_rn(y[t]);
 }
 
 template <int T, bool RECORD>
@@ -549,7 +641,11 @@ __device__ void front_role(const Params &p, uint8_t *smem, Ctrl *ctl,
   const int c = threadIdx.x - kRecThreads;  // channel 0..127
   const int S = p.stages;
   const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
-  float *ssum = reinterpret_cast<float *>(smem + p.scratch_off);  // [T][2][4]
+  float *ssum = reinterpret_cast<float *>(smem + p.scratch_off);   // [T][2][4]
+  float *osum = reinterpret_cast<float *>(smem + p.rscratch_off);  // [T][4]
+  const float nw = bf16_bits_to_float(
+      __ldg(reinterpret_cast<const uint16_t *>(p.norm_weight) + c));
+  bool aborted = false;
   FrontConst fc;
   int cur_head = -1;
   int j = 0;  // live items seen
@@ -557,7 +653,10 @@ __device__ void front_role(const Params &p, uint8_t *smem, Ctrl *ctl,
     const int stage = k % S;
     const uint32_t round = static_cast<uint32_t>(k / S);
     const bool ok = mbar_wait(&ctl->full[stage], round & 1u, &ctl->abort);
-    if (front_sync_or(!ok)) return;
+    if (front_sync_or(!ok)) {
+      aborted = true;
+      break;
+    }
     const int n = n0 + k;
     const int h = n / p.batch;
     const ItemDesc &dsc = desc[stage];
@@ -573,9 +672,14 @@ __device__ void front_role(const Params &p, uint8_t *smem, Ctrl *ctl,
     const int s = j & 1;
     SlotView<T> sv(smem + p.slot_off + s * p.slot_bytes);
     if (j >= 2) {
-      // The recurrence has consumed live item j-2's slot.
+      // The recurrence is done with live item j-2: its outputs, then the slot
+      // takes item j.
       const bool okr = mbar_wait(&ctl->sfree[s], ((j - 2) >> 1) & 1, &ctl->abort);
-      if (front_sync_or(!okr)) return;
+      if (front_sync_or(!okr)) {
+        aborted = true;
+        break;
+      }
+      front_epilogue<T>(p, sv, osum, nw, c);
     }
     if (h != cur_head) {
       load_front_const(p, h, c, fc);
@@ -586,9 +690,122 @@ __device__ void front_role(const Params &p, uint8_t *smem, Ctrl *ctl,
     mbar_arrive(&ctl->fready[s]);
     ++j;
   }
+  // Outputs of the last (up to two) live items.
+  for (int i = (j >= 2 ? j - 2 : 0); i < j && !aborted; ++i) {
+    const bool okr = mbar_wait(&ctl->sfree[i & 1], (i >> 1) & 1, &ctl->abort);
+    if (front_sync_or(!okr)) break;
+    front_epilogue<T>(p, SlotView<T>(smem + p.slot_off + (i & 1) * p.slot_bytes), osum,
+                      nw, c);
+  }
+  // The conv-row stores are complete before the thread that issued them exits.
+  if (T > 1 && c == 0) bulk_wait_all();
 }
 
 // ----------------------------------------------------------------- recurrence
+
+// Passes of the delta rule over the page held in registers (thread (g8, l8):
+// rows g8 + 32m, keys 32cc + 4l8 .. +3).  Each returns, per row m, this
+// thread's partial dot product (x and y halves of the packed accumulator
+// added last); a row's total is the 8-lane reduce_scatter8 of them.
+
+// S *= d; partial rows of S k.
+__device__ __forceinline__ void pass_decay_dot(float4 (&S4)[4][4], const float *d,
+                                               const float *k, int l8, float (&part)[4]) {
+  float2 acc[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) acc[m] = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const int key = 32 * cc + 4 * l8;
+    const float4 d4 = *reinterpret_cast<const float4 *>(d + key);
+    const float4 k4 = *reinterpret_cast<const float4 *>(k + key);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float2 lo = __fmul2_rn(make_float2(S4[m][cc].x, S4[m][cc].y),
+                                   make_float2(d4.x, d4.y));
+      const float2 hi = __fmul2_rn(make_float2(S4[m][cc].z, S4[m][cc].w),
+                                   make_float2(d4.z, d4.w));
+      S4[m][cc] = make_float4(lo.x, lo.y, hi.x, hi.y);
+      acc[m] = __ffma2_rn(lo, make_float2(k4.x, k4.y), acc[m]);
+      acc[m] = __ffma2_rn(hi, make_float2(k4.z, k4.w), acc[m]);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 4; ++m) part[m] = __fadd_rn(acc[m].x, acc[m].y);
+}
+
+// S += k u (u of row m in U[m]); partial rows of S q.
+__device__ __forceinline__ void pass_update_dot(float4 (&S4)[4][4], const float *k,
+                                                const float *q, const float (&U)[4],
+                                                int l8, float (&part)[4]) {
+  float2 acc[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) acc[m] = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const int key = 32 * cc + 4 * l8;
+    const float4 k4 = *reinterpret_cast<const float4 *>(k + key);
+    const float4 q4 = *reinterpret_cast<const float4 *>(q + key);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float2 uu = make_float2(U[m], U[m]);
+      const float2 lo = __ffma2_rn(make_float2(k4.x, k4.y), uu,
+                                   make_float2(S4[m][cc].x, S4[m][cc].y));
+      const float2 hi = __ffma2_rn(make_float2(k4.z, k4.w), uu,
+                                   make_float2(S4[m][cc].z, S4[m][cc].w));
+      S4[m][cc] = make_float4(lo.x, lo.y, hi.x, hi.y);
+      acc[m] = __ffma2_rn(lo, make_float2(q4.x, q4.y), acc[m]);
+      acc[m] = __ffma2_rn(hi, make_float2(q4.z, q4.w), acc[m]);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 4; ++m) part[m] = __fadd_rn(acc[m].x, acc[m].y);
+}
+
+// Token t's update and output dot fused with token t+1's decay and k dot in
+// one sweep over the page: S += k u -> partial rows of S q (opart); S *= dn ->
+// partial rows of S kn (dpart).  Every element and accumulator sees the same
+// operations in the same order as pass_update_dot then pass_decay_dot, so the
+// results are identical; the two row reductions that follow are independent.
+__device__ __forceinline__ void pass_update_dot_decay_dot(
+    float4 (&S4)[4][4], const float *k, const float *q, const float (&U)[4],
+    const float *dn, const float *kn, int l8, float (&opart)[4], float (&dpart)[4]) {
+  float2 oacc[4], dacc[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    oacc[m] = make_float2(0.0f, 0.0f);
+    dacc[m] = make_float2(0.0f, 0.0f);
+  }
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const int key = 32 * cc + 4 * l8;
+    const float4 k4 = *reinterpret_cast<const float4 *>(k + key);
+    const float4 q4 = *reinterpret_cast<const float4 *>(q + key);
+    const float4 d4 = *reinterpret_cast<const float4 *>(dn + key);
+    const float4 n4 = *reinterpret_cast<const float4 *>(kn + key);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float2 uu = make_float2(U[m], U[m]);
+      const float2 lo = __ffma2_rn(make_float2(k4.x, k4.y), uu,
+                                   make_float2(S4[m][cc].x, S4[m][cc].y));
+      const float2 hi = __ffma2_rn(make_float2(k4.z, k4.w), uu,
+                                   make_float2(S4[m][cc].z, S4[m][cc].w));
+      oacc[m] = __ffma2_rn(lo, make_float2(q4.x, q4.y), oacc[m]);
+      oacc[m] = __ffma2_rn(hi, make_float2(q4.z, q4.w), oacc[m]);
+      const float2 lo2 = __fmul2_rn(lo, make_float2(d4.x, d4.y));
+      const float2 hi2 = __fmul2_rn(hi, make_float2(d4.z, d4.w));
+      S4[m][cc] = make_float4(lo2.x, lo2.y, hi2.x, hi2.y);
+      dacc[m] = __ffma2_rn(lo2, make_float2(n4.x, n4.y), dacc[m]);
+      dacc[m] = __ffma2_rn(hi2, make_float2(n4.z, n4.w), dacc[m]);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    opart[m] = __fadd_rn(oacc[m].x, oacc[m].y);
+    dpart[m] = __fadd_rn(dacc[m].x, dacc[m].y);
+  }
+}
+
 
 template <int T, bool RECORD>
 __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
@@ -598,13 +815,6 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
   const int g8 = tid >> 3, l8 = tid & 7;
   const int my_row = g8 + 32 * ((l8 >> 1) & 3);
   const int S = p.stages;
-  const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
-  float *osum = reinterpret_cast<float *>(smem + p.rscratch_off);  // [T][4]
-  // Epilogue mapping: channel ec of token parity et (threads 0-127: even
-  // tokens, 128-255: odd tokens).
-  const int ec = tid & 127, et = tid >> 7, ew = (tid >> 5) & 3;
-  const float nw = bf16_bits_to_float(
-      __ldg(reinterpret_cast<const uint16_t *>(p.norm_weight) + ec));
   const uint64_t pol = policy_evict_first();
   int j = 0;
   uint32_t wq = 0;  // decode: quarters handed to the store thread so far
@@ -655,63 +865,57 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
     SlotView<T> sv(smem + p.slot_off + s * p.slot_bytes);
 
     // The recurrence ("The recurrence").
-#pragma unroll 1
-    for (int t = 0; t < T; ++t) {
-      const float *dt_ = sv.d + t * kDk, *kt = sv.k + t * kDk, *qt = sv.q + t * kDk;
+    if (RECORD) {
+      // No state is written between tokens: token t's update and output sweep
+      // is fused with token t+1's decay and k-dot sweep (same arithmetic).
       float part[4];
-      float2 acc[4];
+      pass_decay_dot(S4, sv.d, sv.k, l8, part);
+      float u = __fmul_rn(
+          __fsub_rn(bf16_bits_to_float(sv.v[my_row]), reduce_scatter8(part, l8)),
+          sv.beta[0]);
+#pragma unroll 1
+      for (int t = 0; t < T; ++t) {
+        if ((l8 & 1) == 0) p.rec_u[(item * T + t) * kDk + my_row] = u;
+        float U[4];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) acc[m] = make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int key = 32 * cc + 4 * l8;
-        const float4 d4 = *reinterpret_cast<const float4 *>(dt_ + key);
-        const float4 k4 = *reinterpret_cast<const float4 *>(kt + key);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float2 lo = __fmul2_rn(make_float2(S4[m][cc].x, S4[m][cc].y),
-                                       make_float2(d4.x, d4.y));
-          const float2 hi = __fmul2_rn(make_float2(S4[m][cc].z, S4[m][cc].w),
-                                       make_float2(d4.z, d4.w));
-          S4[m][cc] = make_float4(lo.x, lo.y, hi.x, hi.y);
-          acc[m] = __ffma2_rn(lo, make_float2(k4.x, k4.y), acc[m]);
-          acc[m] = __ffma2_rn(hi, make_float2(k4.z, k4.w), acc[m]);
+        for (int m = 0; m < 4; ++m)
+          U[m] = __shfl_sync(0xffffffffu, u, (lane & ~7) | (2 * m));
+        const float *kt = sv.k + t * kDk, *qt = sv.q + t * kDk;
+        float opart[4];
+        if (t + 1 < T) {
+          float dpart[4];
+          pass_update_dot_decay_dot(S4, kt, qt, U, sv.d + (t + 1) * kDk,
+                                    sv.k + (t + 1) * kDk, l8, opart, dpart);
+          const float o = reduce_scatter8(opart, l8);
+          const float dot = reduce_scatter8(dpart, l8);
+          if ((l8 & 1) == 0)
+            sv.o[t * kDk + my_row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+          u = __fmul_rn(__fsub_rn(bf16_bits_to_float(sv.v[(t + 1) * kDk + my_row]), dot),
+                        sv.beta[t + 1]);
+        } else {
+          pass_update_dot(S4, kt, qt, U, l8, opart);
+          const float o = reduce_scatter8(opart, l8);
+          if ((l8 & 1) == 0)
+            sv.o[t * kDk + my_row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
         }
       }
+    } else {
+#pragma unroll 1
+      for (int t = 0; t < T; ++t) {
+        const float *kt = sv.k + t * kDk, *qt = sv.q + t * kDk;
+        float part[4];
+        pass_decay_dot(S4, sv.d + t * kDk, kt, l8, part);
+        const float dot = reduce_scatter8(part, l8);
+        const float u = __fmul_rn(
+            __fsub_rn(bf16_bits_to_float(sv.v[t * kDk + my_row]), dot), sv.beta[t]);
+        float U[4];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) part[m] = __fadd_rn(acc[m].x, acc[m].y);
-      const float dot = reduce_scatter8(part, l8);
-      const float u = __fmul_rn(
-          __fsub_rn(bf16_bits_to_float(sv.v[t * kDk + my_row]), dot), sv.beta[t]);
-      if (RECORD && (l8 & 1) == 0) p.rec_u[(item * T + t) * kDk + my_row] = u;
-      float U[4];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) U[m] = __shfl_sync(0xffffffffu, u, (lane & ~7) | (2 * m));
-#pragma unroll
-      for (int m = 0; m < 4; ++m) acc[m] = make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int key = 32 * cc + 4 * l8;
-        const float4 k4 = *reinterpret_cast<const float4 *>(kt + key);
-        const float4 q4 = *reinterpret_cast<const float4 *>(qt + key);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float2 uu = make_float2(U[m], U[m]);
-          const float2 lo = __ffma2_rn(make_float2(k4.x, k4.y), uu,
-                                       make_float2(S4[m][cc].x, S4[m][cc].y));
-          const float2 hi = __ffma2_rn(make_float2(k4.z, k4.w), uu,
-                                       make_float2(S4[m][cc].z, S4[m][cc].w));
-          S4[m][cc] = make_float4(lo.x, lo.y, hi.x, hi.y);
-          acc[m] = __ffma2_rn(lo, make_float2(q4.x, q4.y), acc[m]);
-          acc[m] = __ffma2_rn(hi, make_float2(q4.z, q4.w), acc[m]);
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < 4; ++m) part[m] = __fadd_rn(acc[m].x, acc[m].y);
-      const float o = reduce_scatter8(part, l8);
-      if ((l8 & 1) == 0)
-        sv.o[t * kDk + my_row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-      if (!RECORD) {
+        for (int m = 0; m < 4; ++m)
+          U[m] = __shfl_sync(0xffffffffu, u, (lane & ~7) | (2 * m));
+        pass_update_dot(S4, kt, qt, U, l8, part);
+        const float o = reduce_scatter8(part, l8);
+        if ((l8 & 1) == 0)
+          sv.o[t * kDk + my_row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
         const int tgt = sv.tgt[t];
         if (tgt > 0) {
           float *page_g = p.state + (static_cast<int64_t>(tgt) * p.heads + h) *
@@ -763,36 +967,7 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
         }
       }
     }
-    rec_sync();
-
-    // --- gated RMSNorm epilogue ("Gated RMSNorm"), partial sums of the four
-    // warps of a token combined as KdaWide.quad_sum does.
-    float ov[(T + 1) / 2];
-#pragma unroll
-    for (int i = 0; i < (T + 1) / 2; ++i) {
-      const int t = 2 * i + et;
-      if (t < T) {
-        ov[i] = bf16_bits_to_float(sv.o[t * kDk + ec]);
-        const float tot = warp_sum(__fmul_rn(ov[i], ov[i]));
-        if (lane == 0) osum[t * 4 + ew] = tot;
-      }
-    }
-    rec_sync();
-#pragma unroll
-    for (int i = 0; i < (T + 1) / 2; ++i) {
-      const int t = 2 * i + et;
-      if (t < T) {
-        const float *o4 = osum + t * 4;
-        const float sumsq =
-            __fadd_rn(__fadd_rn(o4[0], o4[2]), __fadd_rn(o4[1], o4[3]));
-        const float var = __fadd_rn(__fmul_rn(sumsq, 1.0f / 128.0f), p.eps);
-        const float rstd = rcp_approx(sqrt_approx(var));
-        const float sg = sigmoid_approx(bf16_bits_to_float(sv.gate[t * kDk + ec]));
-        const float y = __fmul_rn(__fmul_rn(__fmul_rn(ov[i], rstd), nw), sg);
-        p.output[(static_cast<int64_t>(r) * T + t) * dim + h * kDk + ec] =
-            __float2bfloat16_rn(y);
-      }
-    }
+    // o of every token is in the slot; the front applies the gated RMSNorm.
     mbar_arrive(&ctl->sfree[s]);
     if (T > 1 && !RECORD && tid == 0) {
       bulk_wait_read(0);
@@ -915,7 +1090,7 @@ static bool make_layout(int T, int W, bool record, bool conv_f32, int max_smem,
   const uint32_t ctrl = align_up(sizeof(Ctrl), 128);
   const uint32_t descs = align_up(kMaxStages * sizeof(ItemDesc), 128);
   const uint32_t scratch = align_up(T * 8u * 4u, 128);   // front q/k square sums
-  const uint32_t rscratch = align_up(T * 4u * 4u, 128);  // recurrence o square sums
+  const uint32_t rscratch = align_up(T * 4u * 4u, 128);  // front: o square sums
   const uint32_t fixed = ctrl + descs + kSlots * L.slot_bytes + scratch + rscratch;
   const bool ring = T == 1 && !record;
   const int s_max = ring ? 2 : kMaxStages;

@@ -2,7 +2,8 @@
 
 * parity with the oracle's replay on the GPU's own records (exact inputs);
 * record-mode verify followed by replay reproduces, bit for bit, the pages a
-  non-record verify writes (both on the GPU: same operations);
+  non-record verify writes, and record mode's outputs equal the non-record
+  outputs bit for bit (both on the GPU: same operations);
 * padding, error rows and accepted = 0 (copy) write what they should.
 """
 from __future__ import annotations
@@ -40,7 +41,7 @@ def run_step(inp, record):
         rk = torch.zeros((B, H, T, 256), dtype=torch.bfloat16, device="cuda")
     step_from_inputs(d, out, rec_u=ru, rec_kg=rk)()
     torch.cuda.synchronize()
-    return d, ru, rk
+    return d, ru, rk, out
 
 
 def free_slots(o, n):
@@ -60,8 +61,10 @@ def test_record_then_replay_equals_non_record_verify_bitwise(T):
     w = verify_w(T)
     inp = make_inputs(w)
     o = to_oracle(inp)
-    d_plain, _, _ = run_step(inp, record=False)
-    d_rec, ru, rk = run_step(inp, record=True)
+    d_plain, _, _, out_plain = run_step(inp, record=False)
+    d_rec, ru, rk, out_rec = run_step(inp, record=True)
+    # record mode computes the same outputs as the plain verify, bit for bit
+    assert torch.equal(out_rec.view(torch.int16), out_plain.view(torch.int16))
     plain_state = d_plain["state"].cpu().numpy()
     src = src_slots(o)
     dst = free_slots(o, w.batch)
@@ -91,7 +94,7 @@ def test_replay_matches_oracle_on_gpu_records():
     w = verify_w(T, batch=17, heads=6, num_slots=17 * 4 + 40, seed=123)
     inp = make_inputs(w)
     o = to_oracle(inp)
-    d_rec, ru, rk = run_step(inp, record=True)
+    d_rec, ru, rk, _ = run_step(inp, record=True)
     src = src_slots(o)
     dst = free_slots(o, w.batch)
     acc = np.random.default_rng(7).integers(0, T + 1, size=w.batch).astype(np.int32)
@@ -123,7 +126,7 @@ def test_replay_padding_errors_and_copy():
     w = verify_w(T, batch=6, heads=2, num_slots=60, pad=0, seed=5)
     inp = make_inputs(w)
     o = to_oracle(inp)
-    d_rec, ru, rk = run_step(inp, record=True)
+    d_rec, ru, rk, _ = run_step(inp, record=True)
     st = d_rec["state"]
     before = st.clone()
     src = np.array([0, 3, 99, 4, 5, 6], np.int32)
@@ -151,7 +154,7 @@ def test_replay_full_size_record_workload_sampled():
     w = WORKLOADS["verify_q8_record_b64_h64"]
     inp = make_inputs(w)
     o = to_oracle(inp)
-    d_rec, ru, rk = run_step(inp, record=True)
+    d_rec, ru, rk, _ = run_step(inp, record=True)
     B, H, T = w.batch, w.heads, w.tokens
     # replay into a fresh pool region: grow the pool by B slots for the outputs
     st = torch.cat([d_rec["state"], torch.zeros((B, H, 128, 128), device="cuda")])
