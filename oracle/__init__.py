@@ -8,7 +8,9 @@ nothing from there: the two sides share only the seeded input generator.
 The arithmetic lives in ``kda_oracle.c`` (plain C, one scalar loop nest per
 (request, head) item, restating the step of the vLLM API page
 "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.kda.wide", class
-KdaWide).  This module compiles it with gcc (``-ffp-contract=off``, OpenMP when
+KdaWide) and ``oproj_oracle.c`` (the output-projection consumer epilogue of
+the page "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.oproj.consumer",
+class OprojConsumer, per token).  This module compiles it with gcc (``-ffp-contract=off``, OpenMP when
 available) and calls it through ctypes on numpy arrays:
 
 * ``mode="f32"``: every elementary operation correctly rounded to FP32, the
@@ -30,6 +32,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kda_oracle.c")
+_SRC_OPROJ = os.path.join(_HERE, "oproj_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libkda_oracle.so")
 
@@ -74,6 +77,19 @@ class _RecoverArgs(ctypes.Structure):
     ]
 
 
+class _OprojArgs(ctypes.Structure):
+    _fields_ = [
+        ("tp", ctypes.c_int32), ("tokens", ctypes.c_int32),
+        ("hidden", ctypes.c_int32), ("nb", ctypes.c_int32),
+        ("has_delta", ctypes.c_int32),
+        ("partials", _P), ("blocks", _P), ("norm", _P), ("query", _P),
+        ("out_norm", _P), ("prefix", _P), ("output", _P),
+        ("eps", ctypes.c_float), ("out_eps", ctypes.c_float),
+        ("prefix_in", _P), ("pre_out", _P), ("out_pre", _P),
+        ("threads", ctypes.c_int32),
+    ]
+
+
 def _compile(out_path: str) -> None:
     os.makedirs(os.path.dirname(out_path), exist_ok=True)
     base = ["gcc", "-O2", "-std=gnu11", "-fPIC", "-ffp-contract=off",
@@ -82,13 +98,17 @@ def _compile(out_path: str) -> None:
         for omp in (["-fopenmp"], []):
             objs = []
             ok = True
-            for f64 in (0, 1):
-                obj = os.path.join(tmp, f"oracle_f{64 if f64 else 32}.o")
-                cmd = base + omp + [f"-DKDA_ORACLE_F64={f64}", "-c", _SRC, "-o", obj]
-                if subprocess.run(cmd, capture_output=True).returncode != 0:
-                    ok = False
+            for src, macro in ((_SRC, "KDA_ORACLE_F64"), (_SRC_OPROJ, "KDA_OPROJ_F64")):
+                for f64 in (0, 1):
+                    stem = os.path.splitext(os.path.basename(src))[0]
+                    obj = os.path.join(tmp, f"{stem}_f{64 if f64 else 32}.o")
+                    cmd = base + omp + [f"-D{macro}={f64}", "-c", src, "-o", obj]
+                    if subprocess.run(cmd, capture_output=True).returncode != 0:
+                        ok = False
+                        break
+                    objs.append(obj)
+                if not ok:
                     break
-                objs.append(obj)
             if not ok:
                 continue
             tmp_so = os.path.join(tmp, "lib.so")
@@ -100,9 +120,11 @@ def _compile(out_path: str) -> None:
 
 
 def build(force: bool = False) -> str:
-    """Compile ``kda_oracle.c`` into ``oracle/_build/libkda_oracle.so``."""
+    """Compile ``kda_oracle.c`` and ``oproj_oracle.c`` into
+    ``oracle/_build/libkda_oracle.so``."""
     stale = (not os.path.exists(_LIB_PATH)
-             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+             or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(_SRC),
+                                                  os.path.getmtime(_SRC_OPROJ)))
     if force or stale:
         _compile(_LIB_PATH)
     return _LIB_PATH
@@ -124,6 +146,9 @@ def _load():
             rf.restype = ctypes.c_int
             mt = getattr(lib, f"kda_oracle_max_threads_{sfx}")
             mt.restype = ctypes.c_int
+            of = getattr(lib, f"kda_oracle_oproj_{sfx}")
+            of.argtypes = [ctypes.POINTER(_OprojArgs)]
+            of.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -261,3 +286,46 @@ def recover(*, state: np.ndarray, src_slots, dst_slots, accepted, rec_u: np.ndar
     if rc != 0:
         raise ValueError("oracle recover rejected its arguments")
     return st, int(err[0])
+
+
+def oproj(*, partials: np.ndarray, prefix: np.ndarray, out_norm: np.ndarray,
+          blocks: Optional[np.ndarray] = None, norm: Optional[np.ndarray] = None,
+          query: Optional[np.ndarray] = None, has_delta: bool = True,
+          eps: float = 1e-6, out_eps: float = 1e-6, mode: str = "f64",
+          forced_prefix: Optional[np.ndarray] = None, threads: int = 0
+          ) -> Dict[str, np.ndarray]:
+    """Output-projection consumer epilogue (see ``oproj_oracle.c``).
+
+    BF16 arrays as ``numpy.uint16``: ``partials`` [tp, tokens, hidden],
+    ``prefix`` [tokens, hidden] (not modified: the new prefix is returned),
+    ``blocks`` [tokens, nb, hidden] or None, ``norm``/``query``/``out_norm``
+    [hidden].  ``forced_prefix`` replaces the oracle's own new prefix (teacher
+    forcing).  Returns prefix (the new prefix), output, pre (the new prefix
+    before rounding, float64) and out_pre (the output before rounding)."""
+    if mode not in ("f32", "f64"):
+        raise ValueError(mode)
+    lib = _load()
+    u16 = np.uint16
+    part = _c(partials, u16)
+    tp, T, D = part.shape
+    nb = 0 if blocks is None else int(np.asarray(blocks).shape[1])
+    blk = _c(blocks, u16) if nb else None
+    nrm = _c(norm, u16) if nb else None
+    qry = _c(query, u16) if nb else None
+    onrm = _c(out_norm, u16)
+    pref = _c(prefix, u16).copy()
+    out = np.zeros((T, D), dtype=u16)
+    pre = np.zeros((T, D), dtype=np.float64)
+    out_pre = np.zeros((T, D), dtype=np.float64)
+    forced = _c(forced_prefix, u16) if forced_prefix is not None else None
+    a = _OprojArgs()
+    a.tp, a.tokens, a.hidden, a.nb, a.has_delta = tp, T, D, nb, int(bool(has_delta))
+    a.partials, a.blocks, a.norm, a.query = _ptr(part), _ptr(blk), _ptr(nrm), _ptr(qry)
+    a.out_norm, a.prefix, a.output = _ptr(onrm), _ptr(pref), _ptr(out)
+    a.eps, a.out_eps = float(eps), float(out_eps)
+    a.prefix_in, a.pre_out, a.out_pre = _ptr(forced), _ptr(pre), _ptr(out_pre)
+    a.threads = int(threads)
+    rc = getattr(lib, f"kda_oracle_oproj_{mode}")(ctypes.byref(a))
+    if rc != 0:
+        raise ValueError("oracle oproj rejected its arguments")
+    return {"prefix": pref, "output": out, "pre": pre, "out_pre": out_pre}
