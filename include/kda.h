@@ -1,5 +1,7 @@
 /*
- * kda.h -- C ABI of the GB300 (sm_103a) KDA decode / speculative-verify step.
+ * kda.h -- C ABI of the GB300 (sm_103a) KDA decode / speculative-verify step,
+ * its record replay (kda_recover) and the output-projection consumer epilogue
+ * that follows the attention layer (kda_oproj, declared at the end).
  *
  * The operation is the one defined by the vLLM API page
  *   "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.kda.wide"
@@ -49,7 +51,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 2
+#define KDA_ABI_VERSION 3
 #define KDA_DK 128
 #define KDA_MAX_TOKENS 8
 
@@ -177,6 +179,52 @@ typedef struct kda_recover_args {
  * KDA_DEVERR_SLOT / KDA_DEVERR_ACCEPTED and the item writes nothing.  Pages
  * of different requests must be distinct.  One kernel on `stream`. */
 int kda_recover(const kda_recover_args *args, void *stream);
+
+/* Arguments of one output-projection consumer epilogue (kda_oproj). */
+typedef struct kda_oproj_args {
+  int32_t tp;               /* partial outputs per token (TP ranks), 1..64     */
+  int32_t tokens;           /* rows (0 is a no-op)                             */
+  int32_t hidden;           /* features per row: a multiple of 256, <= 7168    */
+  int32_t nb;               /* earlier block outputs per token, 0..8           */
+  int32_t has_delta;        /* nonzero: new prefix = BF16(prefix + BF16(sum)); */
+                            /* zero: new prefix = BF16(sum)                    */
+  const void *partials;     /* bf16 [tp, tokens, hidden]: the partial sums     */
+  const void *blocks;       /* bf16 [tokens, nb, hidden]; NULL when nb == 0    */
+  const void *norm;         /* bf16 [hidden] (nb > 0): block RMSNorm weight    */
+  const void *query;        /* bf16 [hidden] (nb > 0): block query             */
+  const void *out_norm;     /* bf16 [hidden]: output RMSNorm weight            */
+  void *prefix;             /* bf16 [tokens, hidden], in/out: the residual     */
+                            /* stream, replaced by the new prefix              */
+  void *output;             /* bf16 [tokens, hidden], out                      */
+  float eps;                /* epsilon of the block (and prefix) RMS           */
+  float out_eps;            /* epsilon of the output RMSNorm                   */
+} kda_oproj_args;
+
+/* Output-projection consumer epilogue on one GPU: the per-token arithmetic
+ * of class OprojConsumer on the vLLM API page
+ *   "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.oproj.consumer"
+ * (poll_sum, combined_weight, pre, post), with the tensor-parallel partial
+ * outputs read from `partials` instead of remote mailboxes and the whole
+ * hidden vector of a token in one CTA instead of a cluster.  Per token:
+ *   1. sum = the tp partials, summed in FP32 in four rank groups of
+ *      S = max(4, ceil(tp/4)) (each in rank order, then the groups in order);
+ *      p = BF16(sum), or BF16(prefix + BF16(sum)) with has_delta; p is
+ *      written back to `prefix`;
+ *   2. with nb > 0: w = norm * query; logit_b = (v_b . w) * rstd(v_b . v_b,
+ *      eps) for every block and likewise for p; a softmax over the blocks and
+ *      p weights y = sum_b e_b v_b + e_p p;
+ *   3. output = BF16(out_norm * y * rstd(y . y, out_eps)) (y = p when nb == 0),
+ * where rstd(s, e) = 1 / sqrt(s / hidden + e) (a reading: the page uses rstd
+ * without defining it).  FP32 arithmetic; exp and the reciprocal square root
+ * on the hardware's approximate instructions; only the FP32 reduction order
+ * over features differs from a sequential evaluation.  The MoE "latent"
+ * copies and hints of the page's publish step are multi-GPU plumbing and are
+ * not produced.  All pointers are device pointers of the current device with
+ * 16-byte alignment; partials, blocks and prefix must not overlap output.
+ * Errors: KDA_ERR_NULL_ARGS, KDA_ERR_NULL_POINTER, KDA_ERR_SHAPE (sizes
+ * outside the ranges above), KDA_ERR_ALIGNMENT, KDA_ERR_DEVICE,
+ * KDA_ERR_LAUNCH; nothing is launched on error.  One kernel on `stream`. */
+int kda_oproj(const kda_oproj_args *args, void *stream);
 
 /* Static description of a return code (never NULL). */
 const char *kda_strerror(int code);

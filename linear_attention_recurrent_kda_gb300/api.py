@@ -208,3 +208,44 @@ def kda_recover(*, state, src_slots, dst_slots, accepted, rec_u, rec_kg, a_log,
     rc = _lib.call("kda_recover", a, s.cuda_stream)
     if rc != _lib.KDA_SUCCESS:
         raise _lib.KdaError(rc, _lib.strerror(rc))
+
+
+def kda_oproj(*, partials, prefix, output, out_norm, blocks=None, norm=None,
+              query=None, has_delta: bool = True, eps: float = 1e-6,
+              out_eps: float = 1e-6,
+              stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Output-projection consumer epilogue (include/kda.h ``kda_oproj``).
+
+    ``partials`` bf16 [tp, tokens, hidden]; ``prefix`` bf16 [tokens, hidden]
+    (replaced by the new prefix); ``output`` bf16 [tokens, hidden];
+    ``out_norm`` bf16 [hidden]; ``blocks`` bf16 [tokens, nb, hidden] with
+    ``norm``/``query`` bf16 [hidden], or None for no earlier blocks."""
+    bf = torch.bfloat16
+    _check("partials", partials, bf)
+    if partials.dim() != 3:
+        raise ValueError("partials must be [tp, tokens, hidden]")
+    tp, T, D = partials.shape
+    _check("prefix", prefix, bf, (T, D))
+    _check("output", output, bf, (T, D))
+    _check("out_norm", out_norm, bf, (D,))
+    nb = 0
+    if blocks is not None:
+        _check("blocks", blocks, bf)
+        if blocks.dim() != 3 or blocks.shape[0] != T or blocks.shape[2] != D:
+            raise ValueError("blocks must be [tokens, nb, hidden]")
+        nb = blocks.shape[1]
+        _check("norm", norm, bf, (D,))
+        _check("query", query, bf, (D,))
+    a = _lib.KdaOprojArgs()
+    a.tp, a.tokens, a.hidden, a.nb = tp, T, D, nb
+    a.has_delta = int(bool(has_delta))
+    a.partials, a.prefix, a.output = _ptr(partials), _ptr(prefix), _ptr(output)
+    a.out_norm = _ptr(out_norm)
+    a.blocks = _ptr(blocks) if nb else None
+    a.norm = _ptr(norm) if nb else None
+    a.query = _ptr(query) if nb else None
+    a.eps, a.out_eps = float(eps), float(out_eps)
+    s = stream if stream is not None else torch.cuda.current_stream(partials.device)
+    rc = _lib.call("kda_oproj", a, s.cuda_stream)
+    if rc != _lib.KDA_SUCCESS:
+        raise _lib.KdaError(rc, _lib.strerror(rc))

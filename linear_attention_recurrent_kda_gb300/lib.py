@@ -31,7 +31,7 @@ KDA_DEVERR_SLOT = 1
 KDA_DEVERR_ACCEPTED = 2
 KDA_DEVERR_TIMEOUT = 4
 
-EXPORTED = ("kda_decode", "kda_verify", "kda_recover", "kda_strerror",
+EXPORTED = ("kda_decode", "kda_verify", "kda_recover", "kda_oproj", "kda_strerror",
             "kda_abi_version")
 
 
@@ -66,6 +66,18 @@ class KdaRecoverArgs(ctypes.Structure):
     ]
 
 
+class KdaOprojArgs(ctypes.Structure):
+    """Mirror of ``struct kda_oproj_args``."""
+    _fields_ = [
+        ("tp", ctypes.c_int32), ("tokens", ctypes.c_int32),
+        ("hidden", ctypes.c_int32), ("nb", ctypes.c_int32),
+        ("has_delta", ctypes.c_int32),
+        ("partials", _P), ("blocks", _P), ("norm", _P), ("query", _P),
+        ("out_norm", _P), ("prefix", _P), ("output", _P),
+        ("eps", ctypes.c_float), ("out_eps", ctypes.c_float),
+    ]
+
+
 class KdaError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"KDA error {code}: {msg}")
@@ -92,6 +104,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         fn.restype = ctypes.c_int
     lib.kda_recover.argtypes = [ctypes.POINTER(KdaRecoverArgs), ctypes.c_void_p]
     lib.kda_recover.restype = ctypes.c_int
+    lib.kda_oproj.argtypes = [ctypes.POINTER(KdaOprojArgs), ctypes.c_void_p]
+    lib.kda_oproj.restype = ctypes.c_int
     lib.kda_strerror.argtypes = [ctypes.c_int]
     lib.kda_strerror.restype = ctypes.c_char_p
     lib.kda_abi_version.argtypes = []

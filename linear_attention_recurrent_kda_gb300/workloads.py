@@ -171,3 +171,54 @@ def make_inputs(w: Workload) -> Dict[str, object]:
         lower_bound=w.lower_bound, scale=w.scale, eps=w.eps,
     )
     return out
+
+
+# ------------------------------------------- output-projection consumer epilogue
+
+@dataclass(frozen=True)
+class OprojWorkload:
+    """Inputs of the output-projection consumer epilogue (``kda_oproj``).
+
+    Draws (std dev): partials N(0, 0.25) BF16 [tp, tokens, hidden] (a sum of 16
+    is about N(0, 1)); prefix N(0, 1) BF16 [tokens, hidden]; blocks N(0, 1)
+    BF16 [tokens, nb, hidden]; norm U(0.5, 1.5); query N(0, 3/sqrt(hidden)) so
+    that block logits spread over a few units; out_norm U(0.5, 1.5); eps and
+    out_eps 1e-6.
+    """
+    name: str
+    tp: int
+    tokens: int
+    hidden: int
+    nb: int
+    has_delta: bool = True
+    seed: int = 2000
+    eps: float = 1e-6
+    out_eps: float = 1e-6
+
+
+OPROJ_WORKLOADS: Dict[str, OprojWorkload] = {
+    w.name: w
+    for w in (
+        # The page's TP16 consumer at the decode batch of 256 rows.
+        OprojWorkload("oproj_tp16_t256_h7168_nb8", tp=16, tokens=256, hidden=7168,
+                      nb=8, seed=2000),
+    )
+}
+
+
+def make_oproj_inputs(w: OprojWorkload) -> Dict[str, object]:
+    """Draw the inputs of one ``kda_oproj`` call as CPU tensors."""
+    g = torch.Generator().manual_seed(w.seed)
+
+    def randn(*shape, std=1.0):
+        return torch.randn(*shape, generator=g) * std
+
+    out: Dict[str, object] = {}
+    out["partials"] = _bf16(randn(w.tp, w.tokens, w.hidden, std=0.25))
+    out["prefix"] = _bf16(randn(w.tokens, w.hidden))
+    out["blocks"] = _bf16(randn(w.tokens, w.nb, w.hidden)) if w.nb else None
+    out["norm"] = _bf16(torch.rand(w.hidden, generator=g) + 0.5) if w.nb else None
+    out["query"] = _bf16(randn(w.hidden, std=3.0 / w.hidden ** 0.5)) if w.nb else None
+    out["out_norm"] = _bf16(torch.rand(w.hidden, generator=g) + 0.5)
+    out.update(has_delta=bool(w.has_delta), eps=w.eps, out_eps=w.out_eps)
+    return out

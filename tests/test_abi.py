@@ -33,7 +33,7 @@ def test_library_builds_and_exports_every_declared_symbol():
 
 
 def test_version_and_strerror():
-    assert kl.load().kda_abi_version() == 2
+    assert kl.load().kda_abi_version() == 3
     for code in range(0, 12):
         assert kl.strerror(code)
     assert "unknown" in kl.strerror(999)
@@ -81,3 +81,36 @@ def test_alignment_rule_checked_before_any_device_call():
         setattr(a, name, fake)
     a.state = fake + 4            # FP32 pool must be 16-byte aligned
     assert kl.call("kda_decode", a, 0) == kl.KDA_ERR_ALIGNMENT
+
+
+def _oargs(**kw):
+    a = kl.KdaOprojArgs()
+    a.tp, a.tokens, a.hidden, a.nb, a.has_delta = 16, 4, 7168, 2, 1
+    fake = 1 << 20
+    for n in ("partials", "blocks", "norm", "query", "out_norm", "prefix", "output"):
+        setattr(a, n, fake)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(tp=0), kl.KDA_ERR_SHAPE),
+    (dict(tp=65), kl.KDA_ERR_SHAPE),
+    (dict(tokens=-1), kl.KDA_ERR_SHAPE),
+    (dict(nb=9), kl.KDA_ERR_SHAPE),
+    (dict(nb=-1), kl.KDA_ERR_SHAPE),
+    (dict(hidden=7168 + 256), kl.KDA_ERR_SHAPE),
+    (dict(hidden=1000), kl.KDA_ERR_SHAPE),
+    (dict(hidden=0), kl.KDA_ERR_SHAPE),
+    (dict(tokens=0), kl.KDA_SUCCESS),
+    (dict(partials=None), kl.KDA_ERR_NULL_POINTER),
+    (dict(output=None), kl.KDA_ERR_NULL_POINTER),
+    (dict(blocks=None), kl.KDA_ERR_NULL_POINTER),
+    (dict(nb=0, blocks=None, norm=None, query=None, prefix=(1 << 20) + 8),
+     kl.KDA_ERR_ALIGNMENT),
+    (dict(query=(1 << 20) + 2), kl.KDA_ERR_ALIGNMENT),
+])
+def test_oproj_host_validation_without_gpu(kw, code):
+    assert kl.call("kda_oproj", _oargs(**kw), 0) == code
+    assert kl.load().kda_oproj(None, None) == kl.KDA_ERR_NULL_ARGS
