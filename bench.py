@@ -39,6 +39,8 @@ UNIT = "items/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCE = os.path.join(ROOT, "linear_attention_recurrent_kda_gb300", "csrc",
                              "kda_step.cu")
+OPROJ_SOURCE = os.path.join(ROOT, "linear_attention_recurrent_kda_gb300", "csrc",
+                            "kda_oproj.cu")
 
 
 def dist_env():
@@ -71,21 +73,21 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sha():
-    with open(KERNEL_SOURCE, "rb") as f:
+def kernel_sha(source: str = None):
+    with open(source or KERNEL_SOURCE, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def ncu_traffic(workload: str):
+def ncu_traffic(workload: str, kernel: str = "kda_step", source: str = None):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
     workload, or None when absent or taken on a different kernel source."""
-    path = os.path.join(ROOT, "profiles", f"kda_step_{workload}.ncu.json")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.ncu.json")
     try:
         with open(path) as f:
             p = json.load(f)
     except Exception:
         return None
-    if p.get("source_sha256") != kernel_sha():
+    if p.get("source_sha256") != kernel_sha(source):
         return None
     return p.get("dram_bytes_per_launch")
 
@@ -268,6 +270,115 @@ def run_recover(args):
                      "algorithmic_bytes_per_launch": nbytes}}), flush=True)
 
 
+def run_oproj(args):
+    """Times kda_oproj (the output-projection consumer epilogue) on the TP16,
+    256-row, hidden 7168, 8-block workload (single GPU).  Its inputs (~95 MB)
+    fit in L2, so a 256 MiB buffer is written between launches and only the
+    launches are timed (CUDA events around each one on the launching stream).
+    The prefix is updated in place every step, as the layer does."""
+    import torch
+    from linear_attention_recurrent_kda_gb300.api import kda_oproj
+    from linear_attention_recurrent_kda_gb300.workloads import (OPROJ_WORKLOADS,
+                                                                make_oproj_inputs)
+    w = OPROJ_WORKLOADS["oproj_tp16_t256_h7168_nb8"]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    host = make_oproj_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    out = torch.empty((w.tokens, w.hidden), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        kda_oproj(partials=d["partials"], prefix=d["prefix"], output=out,
+                  out_norm=d["out_norm"], blocks=d["blocks"], norm=d["norm"],
+                  query=d["query"], has_delta=w.has_delta, eps=w.eps,
+                  out_eps=w.out_eps, stream=stream)
+
+    steps = min(args.steps, 2000)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    t_w0 = time.time()
+    while time.time() - t_w0 < 1.0:          # untimed soak: clock samples under load
+        for _ in range(50):
+            flush.zero_()
+            call()
+        torch.cuda.synchronize()
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t_w1 = time.time()
+    sampler.stop()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+    row = w.hidden * 2
+    rows = w.tp + w.nb + (1 if w.has_delta else 0) + 2   # reads + prefix/output writes
+    nbytes = w.tokens * rows * row + 3 * row
+    peak, kind = measured_peak()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "output-projection consumer epilogue rows/s", "op": "oproj",
+        "value": w.tokens / (ms * 1e-3), "unit": "rows/s", "ms_per_step": ms,
+        "steps": steps, "warmup": max(args.warmup, 3), "higher_is_better": True,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "tp": w.tp, "tokens": w.tokens,
+                   "hidden": w.hidden, "nb": w.nb, "has_delta": w.has_delta,
+                   "l2": "inputs fit in L2: a 256 MiB buffer is written between "
+                         "launches; only the launches are timed"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "peak_source": f"{kind} hbm_gbs",
+                     "traffic": ncu_traffic(w.name, "kda_oproj", OPROJ_SOURCE),
+                     "algorithmic_bytes_per_launch": nbytes},
+        "clocks": dict(sampler.summary(t_w0, t_w1) or {}, window="soak+timed"),
+        "gpu_launches": steps,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oproj_cpu_baseline(w, host, ms)
+    print(json.dumps(line), flush=True)
+
+
+def oproj_cpu_baseline(w, host, gpu_ms):
+    """The oracle (FP32 mode, page order) on the host cores, on the first 64
+    rows of the same inputs, scaled to rows/s."""
+    import oracle
+    n = min(64, w.tokens)
+
+    def bits(t):
+        return None if t is None else t[:n].contiguous().view(torch_int16()).numpy().view("uint16")
+
+    args = dict(partials=host["partials"][:, :n].contiguous().view(torch_int16()).numpy()
+                .view("uint16"), prefix=bits(host["prefix"]),
+                out_norm=host["out_norm"].view(torch_int16()).numpy().view("uint16"),
+                blocks=bits(host["blocks"]),
+                norm=host["norm"].view(torch_int16()).numpy().view("uint16"),
+                query=host["query"].view(torch_int16()).numpy().view("uint16"),
+                has_delta=w.has_delta, eps=w.eps, out_eps=w.out_eps, mode="f32")
+    oracle.oproj(**args)
+    t0 = time.time()
+    reps = 0
+    while time.time() - t0 < 5.0:
+        oracle.oproj(**args)
+        reps += 1
+    sec = (time.time() - t0) / reps
+    return {"value": n / sec, "unit": "rows/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "sample": f"first {n} of {w.tokens} rows, FP32 mode, "
+                                        f"{reps} repetitions"}
+
+
+def torch_int16():
+    import torch
+    return torch.int16
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -276,9 +387,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="decode_b256_h32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "recover"],
+    ap.add_argument("--op", default="step", choices=["step", "recover", "oproj"],
                     help="step: the decode/verify step (default); recover: the "
-                         "record replay after a record-mode verify")
+                         "record replay after a record-mode verify; oproj: the "
+                         "output-projection consumer epilogue")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -292,6 +404,9 @@ def main():
         return
     if args.op == "recover":
         run_recover(args)
+        return
+    if args.op == "oproj":
+        run_oproj(args)
         return
 
     import torch
