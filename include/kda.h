@@ -226,6 +226,15 @@ typedef struct kda_oproj_args {
  * KDA_ERR_LAUNCH; nothing is launched on error.  One kernel on `stream`. */
 int kda_oproj(const kda_oproj_args *args, void *stream);
 
+/* Self-test of the bounded on-chip waits that every kernel above uses: one
+ * CTA waits on an mbarrier that nothing completes; the wait gives up after
+ * its wall-clock limit (2 s), KDA_DEVERR_TIMEOUT is OR-ed into *err (a
+ * device word, 4-byte aligned) and the kernel returns -- no trap, no fault,
+ * the context stays usable.  For failure-detection tests.  Returns
+ * KDA_ERR_NULL_POINTER / KDA_ERR_ALIGNMENT / KDA_ERR_LAUNCH or KDA_SUCCESS;
+ * one kernel on `stream`. */
+int kda_selftest_wait_timeout(int32_t *err, void *stream);
+
 /* Static description of a return code (never NULL). */
 const char *kda_strerror(int code);
 

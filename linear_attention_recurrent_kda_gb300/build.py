@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(HERE, "libkda_gb300.so")
 SOURCES = [os.path.join(CSRC, n) for n in ("kda_step.cu", "kda_split.cu",
-                                            "kda_recover.cu", "kda_oproj.cu")]
+                                            "kda_recover.cu", "kda_oproj.cu",
+                                            "kda_selftest.cu")]
 HEADERS = [os.path.join(INCLUDE, "kda.h"), os.path.join(CSRC, "kda_device.cuh")]
 
 NVCC_FLAGS = [

@@ -31,8 +31,8 @@ KDA_DEVERR_SLOT = 1
 KDA_DEVERR_ACCEPTED = 2
 KDA_DEVERR_TIMEOUT = 4
 
-EXPORTED = ("kda_decode", "kda_verify", "kda_recover", "kda_oproj", "kda_strerror",
-            "kda_abi_version")
+EXPORTED = ("kda_decode", "kda_verify", "kda_recover", "kda_oproj",
+            "kda_selftest_wait_timeout", "kda_strerror", "kda_abi_version")
 
 
 class KdaArgs(ctypes.Structure):
@@ -106,6 +106,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.kda_recover.restype = ctypes.c_int
     lib.kda_oproj.argtypes = [ctypes.POINTER(KdaOprojArgs), ctypes.c_void_p]
     lib.kda_oproj.restype = ctypes.c_int
+    lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.kda_selftest_wait_timeout.restype = ctypes.c_int
     lib.kda_strerror.argtypes = [ctypes.c_int]
     lib.kda_strerror.restype = ctypes.c_char_p
     lib.kda_abi_version.argtypes = []

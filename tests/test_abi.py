@@ -114,3 +114,11 @@ def _oargs(**kw):
 def test_oproj_host_validation_without_gpu(kw, code):
     assert kl.call("kda_oproj", _oargs(**kw), 0) == code
     assert kl.load().kda_oproj(None, None) == kl.KDA_ERR_NULL_ARGS
+
+
+def test_selftest_host_validation_without_gpu():
+    import ctypes
+    lib = kl.load()
+    assert lib.kda_selftest_wait_timeout(None, None) == kl.KDA_ERR_NULL_POINTER
+    assert lib.kda_selftest_wait_timeout(ctypes.c_void_p((1 << 20) + 2), None) == \
+        kl.KDA_ERR_ALIGNMENT
