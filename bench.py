@@ -208,7 +208,7 @@ def cpu_baseline(workload, budget_s=12.0):
     n = min(workload.items, 1024)
     items = np.sort(rng.choice(workload.items, size=n, replace=False)).astype(np.int32)
     done, t0 = 0, time.perf_counter()
-    while time.perf_counter() - t0 < budget_s and done < 64 * n:
+    while time.perf_counter() - t0 < budget_s:
         oracle.run(inp, mode="f32", items=items, in_place=True, threads=threads)
         done += n
     dt = time.perf_counter() - t0
@@ -365,7 +365,7 @@ def oproj_cpu_baseline(w, host, gpu_ms):
     oracle.oproj(**args)
     t0 = time.time()
     reps = 0
-    while time.time() - t0 < 5.0:
+    while time.time() - t0 < 10.0:
         oracle.oproj(**args)
         reps += 1
     sec = (time.time() - t0) / reps
