@@ -140,6 +140,27 @@ def test_record_mode(tokens, gate_mode, has_bias):
     check(w)
 
 
+@pytest.mark.parametrize("record", [False, True])
+@pytest.mark.parametrize("tokens", [2, 3, 4, 5, 6, 7, 8])
+def test_every_token_count_with_a_wide_window(tokens, record):
+    """Every verify instantiation (T = 2..8, with and without records), the
+    conv window wider than T + 2 (the extra columns keep their values)."""
+    extra = 1 + tokens % 3
+    if record:
+        w = small(tokens=tokens, slot_layout="checkpoint", conv_width=tokens + 2 + extra,
+                  record=True, gate_mode=tokens % 2, has_bias=tokens % 3 == 0, batch=11,
+                  heads=5, num_slots=14, pad=1, seed=200 + tokens)
+    else:
+        w = small(tokens=tokens, slot_layout="verify", conv_width=tokens + 2 + extra,
+                  gate_mode=tokens % 2, has_bias=tokens % 3 == 1, batch=11, heads=5,
+                  num_slots=11 * tokens + 2, pad=1, seed=220 + tokens)
+    check(w)
+
+
+def test_many_heads_decode():
+    check(small(batch=3, heads=96, num_slots=8, pad=0, seed=240))
+
+
 def test_gate_mode_1_and_bias_decode():
     check(small(gate_mode=1, has_bias=True, seed=60))
 
