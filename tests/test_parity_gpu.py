@@ -157,6 +157,35 @@ def test_every_token_count_with_a_wide_window(tokens, record):
     check(w)
 
 
+@pytest.mark.parametrize("case", ["x_saturated", "x_zero", "state_large", "beta_saturated"])
+@pytest.mark.parametrize("tokens", [1, 4])
+def test_extreme_inputs(case, tokens):
+    """Inputs at the edges of the functions' ranges: SiLU saturated (x * 20),
+    all-zero x (q = k = 0: the L2 norms fall back on their 1e-6), state pages
+    scaled by 100, beta logits of +-20 (sigmoid saturated)."""
+    if tokens == 1:
+        w = small(batch=13, heads=4, num_slots=20, pad=1, seed=260)
+    else:
+        w = small(tokens=4, slot_layout="verify", conv_width=6, batch=9, heads=3,
+                  num_slots=9 * 4 + 2, pad=1, seed=261)
+
+    def mutate(inp):
+        if case == "x_saturated":
+            inp["x"] = (inp["x"].float() * 20.0).to(torch.bfloat16)
+        elif case == "x_zero":
+            inp["x"] = torch.zeros_like(inp["x"])
+            inp["conv_state"] = torch.zeros_like(inp["conv_state"])
+            if inp.get("conv_bias") is not None:
+                inp["conv_bias"] = torch.zeros_like(inp["conv_bias"])
+        elif case == "state_large":
+            inp["state"] = inp["state"] * 100.0
+        else:
+            sign = torch.where(torch.arange(inp["beta"].numel()) % 2 == 0, 1.0, -1.0)
+            inp["beta"] = (sign.view_as(inp["beta"]) * 20.0).to(torch.bfloat16)
+
+    check(w, mutate)
+
+
 def test_many_heads_decode():
     check(small(batch=3, heads=96, num_slots=8, pad=0, seed=240))
 
