@@ -311,6 +311,48 @@ __device__ __forceinline__ void warp_sum_n(float (&v)[N]) {
       v[i] = __fadd_rn(v[i], __shfl_xor_sync(0xffffffffu, v[i], s));
 }
 
+// Warp sums of N values (N a power of two <= 32), scattered: lane L ends up
+// with the total of value (L / (32 / N)) % N.  Each level halves the values a
+// lane keeps and adds its partner's copy of the same values (xor distance 16,
+// 8, ... ), then the remaining levels add the partner's single value; every
+// total is the same pairwise tree as warp_sum's, so the bits are identical.
+template <int N>
+__device__ __forceinline__ float warp_reduce_scatter(const float (&v)[N], int lane) {
+  static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "N must be a power of two <= 32");
+  float cur[N];
+#pragma unroll
+  for (int j = 0; j < N; ++j) cur[j] = v[j];
+  int n = N;
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    if (n > 1) {
+      const int h = n >> 1;
+      const bool hi = (lane & s) != 0;
+#pragma unroll
+      for (int j = 0; j < N / 2; ++j) {
+        if (j < h) {
+          const float keep = hi ? cur[j + h] : cur[j];
+          const float send = hi ? cur[j] : cur[j + h];
+          cur[j] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, s));
+        }
+      }
+      n = h;
+    } else {
+      cur[0] = __fadd_rn(cur[0], __shfl_xor_sync(0xffffffffu, cur[0], s));
+    }
+  }
+  return cur[0];
+}
+
+template <int X>
+struct NextPow2 {
+  static constexpr int value = X <= 1 ? 1 : 2 * NextPow2<(X + 1) / 2>::value;
+};
+template <>
+struct NextPow2<1> {
+  static constexpr int value = 1;
+};
+
 // Sum over the 8 lanes of a row group of four partial sums (one per value row
 // m = 0..3); returns the total of row (lane >> 1) & 3.
 __device__ __forceinline__ float reduce_scatter8(const float (&x)[4], int l) {

@@ -452,7 +452,10 @@ __device__ __forceinline__ void front_item(const Params &p, uint8_t *st,
       y[part][t] = bf16_round(silu_approx(acc));
     }
   }
-  float sq[2 * T];
+  constexpr int NS = NextPow2<2 * T>::value;  // square sums, padded with zeros
+  float sq[NS];
+#pragma unroll
+  for (int i = 2 * T; i < NS; ++i) sq[i] = 0.0f;
 #pragma unroll
   for (int t = 0; t < T; ++t) {
     sv.q[t * kDk + c] = y[0][t];
@@ -469,10 +472,11 @@ __device__ __forceinline__ void front_item(const Params &p, uint8_t *st,
       for (int t = 0; t < T; ++t)
         p.dbg[((item * T + t) * 4 + part) * kDk + c] = __float2bfloat16_rn(y[part][t]);
   }
-  warp_sum_n(sq);
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < 2 * T; ++i) ssum[i * 4 + fw] = sq[i];
+  {
+    // Each lane ends with one warp total (the same tree as a butterfly).
+    const float tot = warp_reduce_scatter<NS>(sq, lane);
+    const int idx = (lane / (32 / NS)) % NS;
+    if (idx < 2 * T && lane % (32 / NS) == 0) ssum[idx * 4 + fw] = tot;
   }
   // The rewritten conv rows are read next by the async proxy (bulk stores).
   if (T > 1) fence_proxy_async_smem();
@@ -607,17 +611,20 @@ __device__ __forceinline__ void front_epilogue(const Params &p, const SlotView<T
   const int h = n / p.batch;
   const int r = n - h * p.batch;
   const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
-  float ov[T], gv[T], tot[T];
+  constexpr int NE = NextPow2<T>::value;
+  float ov[T], gv[T], sq[NE];
+#pragma unroll
+  for (int t = T; t < NE; ++t) sq[t] = 0.0f;
 #pragma unroll
   for (int t = 0; t < T; ++t) {
     ov[t] = bf16_bits_to_float(sv.o[t * kDk + c]);
     gv[t] = bf16_bits_to_float(sv.gate[t * kDk + c]);
-    tot[t] = __fmul_rn(ov[t], ov[t]);
+    sq[t] = __fmul_rn(ov[t], ov[t]);
   }
-  warp_sum_n(tot);
-  if (lane == 0) {
-#pragma unroll
-    for (int t = 0; t < T; ++t) osum[t * 4 + fw] = tot[t];
+  {
+    const float tot = warp_reduce_scatter<NE>(sq, lane);
+    const int idx = (lane / (32 / NE)) % NE;
+    if (idx < T && lane % (32 / NE) == 0) osum[idx * 4 + fw] = tot;
   }
   front_sync();
   float y[T];
