@@ -418,7 +418,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    from linear_attention_recurrent_kda_gb300.accounting import step_bytes
+    from linear_attention_recurrent_kda_gb300.accounting import (
+        RECURRENCE_FLOP_PER_TOKEN_ITEM, recurrence_flop, step_bytes)
     from linear_attention_recurrent_kda_gb300.api import step_from_inputs
     from linear_attention_recurrent_kda_gb300.workloads import make_inputs
 
@@ -551,6 +552,12 @@ def main():
     achieved = nbytes["total"] / (kern_ms * 1e-3) / 1e9
     state_gbs = nbytes["state"] / (kern_ms * 1e-3) / 1e9
     traffic = ncu_traffic(w.name if rank == 0 else workload.name)
+    # FP32 pipe: the recurrence's flop against the derived non-tensor FP32 peak
+    # (SMs x 128 FP32 lanes x 2 flop per FMA x the maximum SM clock).
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    max_mhz = float((clocks or {}).get("sm_max_mhz") or 2070.0)
+    fp32_peak = sms * 128 * 2 * max_mhz * 1e6 / 1e12
+    fp32_tf = recurrence_flop(w, host) / (kern_ms * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -569,6 +576,11 @@ def main():
                      "state_bytes_per_launch": nbytes["state"],
                      "state_gbs": state_gbs, "state_frac": state_gbs / peak,
                      "kernel_ms": kern_ms},
+        "fp32_pipe": {"achieved": fp32_tf, "peak": fp32_peak, "unit": "TFLOP/s",
+                      "frac": fp32_tf / fp32_peak,
+                      "flop_per_token_item": RECURRENCE_FLOP_PER_TOKEN_ITEM,
+                      "peak_source": f"derived: {sms} SMs x 128 FP32 lanes x 2 flop x "
+                                     f"{max_mhz:.0f} MHz"},
         "clocks": dict(clocks or {}, window=clock_window),
         "e2e": {"value": items / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -53,3 +53,24 @@ def step_bytes(w: Workload, inputs: Dict[str, object]) -> Dict[str, int]:
     other = conv + x + gate + out + fa + per_head + rec + tables
     return {"state": state_read + state_write, "other": other,
             "total": state_read + state_write + other}
+
+
+# FP32 work of one token of one live item in the recurrence (per key j and
+# value row i: S *= d, S k, S += k u, S q): 16,384 multiplies + 3 x 16,384
+# fused multiply-adds at 2 flop each.
+RECURRENCE_FLOP_PER_TOKEN_ITEM = 128 * 128 + 3 * 128 * 128 * 2
+
+
+def recurrence_flop(w: Workload, inputs: Dict[str, object]) -> int:
+    """FP32 recurrence flop of one step of ``w``: live items x tokens x
+    RECURRENCE_FLOP_PER_TOKEN_ITEM (padding and error items do no work)."""
+    B, H, T = w.batch, w.heads, w.tokens
+    slots = inputs["slots"]
+    if T == 1:
+        live_req = int((slots > 0).sum())
+    else:
+        acc = inputs["accepted"].to(torch.int64)
+        ok = (acc >= 1) & (acc <= T)
+        sel = slots.gather(1, (acc.clamp(1, T) - 1).view(B, 1)).view(B)
+        live_req = int(((sel > 0) & ok).sum())
+    return live_req * H * T * RECURRENCE_FLOP_PER_TOKEN_ITEM
