@@ -346,6 +346,56 @@ def run_oproj(args):
     print(json.dumps(line), flush=True)
 
 
+def run_pattern(args):
+    """The decode workload's page traffic alone (kda_probe_page_copy: every
+    page read into shared memory and written back in place, the step's
+    schedule, no arithmetic), with the step's two stages and with three: the
+    bandwidth ceiling of that access pattern, beside the measured copy peak."""
+    import torch
+    from linear_attention_recurrent_kda_gb300.api import kda_probe_page_copy
+    from linear_attention_recurrent_kda_gb300.workloads import WORKLOADS, make_inputs
+
+    w = WORKLOADS[args.workload or "decode_b256_h32"]
+    if w.tokens != 1:                      # the probe follows decode's one page per item
+        w = WORKLOADS["decode_b256_h32"]
+    host = make_inputs(w)
+    dev = torch.device("cuda", 0)
+    state, slots = host["state"].to(dev), host["slots"].to(dev)
+    live = int((host["slots"] > 0).sum()) * w.heads
+    nbytes = live * 2 * 128 * 128 * 4
+    stream = torch.cuda.Stream(device=dev)
+    peak, peak_kind = measured_peak()
+    res = {}
+    for stages in (2, 3):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                kda_probe_page_copy(state=state, slots=slots, stages=stages, stream=stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                kda_probe_page_copy(state=state, slots=slots, stages=stages, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / args.steps
+        res[stages] = (ms, nbytes / (ms * 1e-3) / 1e9)
+    ms2, gbs2 = res[2]
+    line = {
+        "metric": "decode page access pattern (read + write back in place, no arithmetic)",
+        "value": gbs2, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms2, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name + " pages", "stages": 2, "live_items": live,
+                   "l2": "inputs larger than L2 (1 GiB of pages per step); no flush"},
+        "roofline": {"bound": "hbm", "achieved": gbs2, "peak": peak, "unit": "GB/s",
+                     "frac": gbs2 / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": nbytes},
+        "three_stages": {"ms_per_step": res[3][0], "achieved": res[3][1],
+                         "frac": res[3][1] / peak},
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def oproj_cpu_baseline(w, host, gpu_ms):
     """The oracle (FP32 mode, page order) on the host cores, on the first 64
     rows of the same inputs, scaled to rows/s."""
@@ -387,10 +437,12 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="decode_b256_h32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "recover", "oproj"],
+    ap.add_argument("--op", default="step",
+                    choices=["step", "recover", "oproj", "pattern"],
                     help="step: the decode/verify step (default); recover: the "
                          "record replay after a record-mode verify; oproj: the "
-                         "output-projection consumer epilogue")
+                         "output-projection consumer epilogue; pattern: the decode "
+                         "workload's page traffic alone (bandwidth ceiling probe)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -405,6 +457,8 @@ def main():
     if args.op == "recover":
         run_recover(args)
         return
+    if args.op == "pattern":
+        return run_pattern(args)
     if args.op == "oproj":
         run_oproj(args)
         return

@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 3
+#define KDA_ABI_VERSION 4
 #define KDA_DK 128
 #define KDA_MAX_TOKENS 8
 
@@ -225,6 +225,30 @@ typedef struct kda_oproj_args {
  * outside the ranges above), KDA_ERR_ALIGNMENT, KDA_ERR_DEVICE,
  * KDA_ERR_LAUNCH; nothing is launched on error.  One kernel on `stream`. */
 int kda_oproj(const kda_oproj_args *args, void *stream);
+
+/* Measurement probe: the decode step's HBM access pattern without its
+ * arithmetic.  For every (request r, head h) item (item n = h * batch + r,
+ * the step's order) whose slots[r] is in 1..num_slots-1, the 64 KiB FP32
+ * page state[slots[r], h] is read into shared memory by one TMA bulk copy
+ * and written back to the same address by one bulk store; one CTA per SM
+ * over contiguous item ranges with a ring of `stages` (2 or 3) pages, as
+ * the step schedules its pages.  The pool's values are unchanged.  Its
+ * bandwidth bounds what the step's page traffic can reach.
+ *   state  float [num_slots, heads, 128, 128], 16-byte aligned, in/out
+ *   slots  int32 [batch] (device); <= 0 skips the item; >= num_slots skips
+ *          it and sets KDA_DEVERR_SLOT in *err
+ *   err    optional device word (4-byte aligned) for KDA_DEVERR_* flags
+ * Errors: KDA_ERR_NULL_ARGS, KDA_ERR_SHAPE (negative sizes, num_slots < 1,
+ * stages outside 2..3), KDA_ERR_NULL_POINTER, KDA_ERR_ALIGNMENT,
+ * KDA_ERR_DEVICE, KDA_ERR_LAUNCH; nothing is launched on error.  One kernel
+ * on `stream`. */
+typedef struct kda_probe_args {
+  int32_t batch, heads, num_slots, stages;
+  float *state;
+  const int32_t *slots;
+  int32_t *err;
+} kda_probe_args;
+int kda_probe_page_copy(const kda_probe_args *args, void *stream);
 
 /* Self-test of the bounded on-chip waits that every kernel above uses: one
  * CTA waits on an mbarrier that nothing completes; the wait gives up after

@@ -249,3 +249,26 @@ def kda_oproj(*, partials, prefix, output, out_norm, blocks=None, norm=None,
     rc = _lib.call("kda_oproj", a, s.cuda_stream)
     if rc != _lib.KDA_SUCCESS:
         raise _lib.KdaError(rc, _lib.strerror(rc))
+
+
+def kda_probe_page_copy(*, state, slots, stages: int = 2, err=None,
+                        stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Access-pattern probe (include/kda.h ``kda_probe_page_copy``): every
+    (request, head) page of ``state`` (float32 [num_slots, heads, 128, 128])
+    named by ``slots`` (int32 [batch]) is read into shared memory and written
+    back in place, with the decode step's schedule and no arithmetic."""
+    _check("state", state, torch.float32)
+    if state.dim() != 4 or tuple(state.shape[2:]) != (128, 128):
+        raise ValueError("state must be [num_slots, heads, 128, 128]")
+    _check("slots", slots, torch.int32)
+    if slots.dim() != 1:
+        raise ValueError("slots must be [batch]")
+    a = _lib.KdaProbeArgs()
+    a.batch, a.heads, a.num_slots, a.stages = (slots.shape[0], state.shape[1],
+                                               state.shape[0], int(stages))
+    a.state, a.slots = _ptr(state), _ptr(slots)
+    a.err = _ptr(err) if err is not None else None
+    s = stream if stream is not None else torch.cuda.current_stream(state.device)
+    rc = _lib.call("kda_probe_page_copy", a, s.cuda_stream)
+    if rc != _lib.KDA_SUCCESS:
+        raise _lib.KdaError(rc, _lib.strerror(rc))

@@ -1,8 +1,10 @@
 """Build the in-tree CUDA library ``libkda_gb300.so`` for sm_103a.
 
-One translation unit (csrc/kda_step.cu) compiled by nvcc with a single
-``-gencode arch=compute_103a,code=sm_103a``; the result sits next to this file
-and is loaded by ``linear_attention_recurrent_kda_gb300.lib``.
+The translation units of csrc/ (the step, split, replay, output-projection,
+self-test and probe kernels) compiled by nvcc in parallel with a single
+``-gencode arch=compute_103a,code=sm_103a`` and linked into one shared
+library, which sits next to this file and is loaded by
+``linear_attention_recurrent_kda_gb300.lib``.
 """
 from __future__ import annotations
 
@@ -18,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(HERE, "libkda_gb300.so")
 SOURCES = [os.path.join(CSRC, n) for n in ("kda_step.cu", "kda_split.cu",
                                             "kda_recover.cu", "kda_oproj.cu",
-                                            "kda_selftest.cu")]
+                                            "kda_selftest.cu", "kda_probe.cu")]
 HEADERS = [os.path.join(INCLUDE, "kda.h"), os.path.join(CSRC, "kda_device.cuh")]
 
 NVCC_FLAGS = [

@@ -33,7 +33,7 @@ def test_library_builds_and_exports_every_declared_symbol():
 
 
 def test_version_and_strerror():
-    assert kl.load().kda_abi_version() == 3
+    assert kl.load().kda_abi_version() == 4
     for code in range(0, 12):
         assert kl.strerror(code)
     assert "unknown" in kl.strerror(999)
@@ -122,3 +122,29 @@ def test_selftest_host_validation_without_gpu():
     assert lib.kda_selftest_wait_timeout(None, None) == kl.KDA_ERR_NULL_POINTER
     assert lib.kda_selftest_wait_timeout(ctypes.c_void_p((1 << 20) + 2), None) == \
         kl.KDA_ERR_ALIGNMENT
+
+
+def _pargs(**kw):
+    a = kl.KdaProbeArgs()
+    a.batch, a.heads, a.num_slots, a.stages = 4, 2, 8, 2
+    a.state, a.slots = 1 << 20, 1 << 21
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(stages=1), kl.KDA_ERR_SHAPE),
+    (dict(stages=4), kl.KDA_ERR_SHAPE),
+    (dict(batch=-1), kl.KDA_ERR_SHAPE),
+    (dict(num_slots=0), kl.KDA_ERR_SHAPE),
+    (dict(batch=0), kl.KDA_SUCCESS),
+    (dict(state=None), kl.KDA_ERR_NULL_POINTER),
+    (dict(slots=None), kl.KDA_ERR_NULL_POINTER),
+    (dict(state=(1 << 20) + 4), kl.KDA_ERR_ALIGNMENT),
+    (dict(slots=(1 << 21) + 2), kl.KDA_ERR_ALIGNMENT),
+    (dict(err=(1 << 22) + 1), kl.KDA_ERR_ALIGNMENT),
+])
+def test_probe_host_validation_without_gpu(kw, code):
+    assert kl.call("kda_probe_page_copy", _pargs(**kw), 0) == code
+    assert kl.load().kda_probe_page_copy(None, None) == kl.KDA_ERR_NULL_ARGS
