@@ -14,11 +14,13 @@
 //
 // Design: persistent, one CTA per SM, items (request, head) in head-major
 // contiguous ranges.  Warp 8 lane 0 (producer) stages each item's checkpoint
-// page and its records into a 3-stage shared-memory ring with TMA bulk copies
-// and, once the compute warps have written the replayed page back into the
-// stage, stores it with one TMA bulk store and reuses the stage after the copy
-// has read it.  Warps 0-7 hold the page in registers (thread (g, l): keys
-// {32c + 4l + e} of value rows g + 32m) and replay the tokens.
+// page and the records of its accepted tokens into a 3-stage shared-memory
+// ring with TMA bulk copies and, once the compute warps have written the
+// replayed page back into the stage, stores it with one TMA bulk store and
+// reuses the stage after the copy has read it.  Warps 0-7 first form k_hat
+// and the decay of every accepted token (two barriers per item), then hold
+// the page in registers (thread (g, l): keys {32c + 4l + e} of value rows
+// g + 32m) and sweep the tokens with no barrier between them.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -127,14 +129,16 @@ __device__ void producer(const Params &p, uint8_t *smem, Ctrl *ctl, Desc *desc,
       const int h = (n0 + k) / p.batch;
       const int r = (n0 + k) - h * p.batch;
       const int64_t item = static_cast<int64_t>(r) * p.heads + h;
-      const uint32_t rec_bytes = static_cast<uint32_t>(p.tokens) * kDk * 4u;
+      const uint32_t rec_bytes = static_cast<uint32_t>(d.accepted) * kDk * 4u;
       mbar_arrive_expect_tx(&ctl->full[stage], kPageBytes + 2u * rec_bytes);
       bulk_g2s_hint(st, p.state + (static_cast<int64_t>(d.src) * p.heads + h) * page_elems,
                     kPageBytes, &ctl->full[stage], pol);
-      bulk_g2s(st + p.kg_off, p.rec_kg + item * p.tokens * 2 * kDk, rec_bytes,
-               &ctl->full[stage]);
-      bulk_g2s(st + p.u_off, p.rec_u + item * p.tokens * kDk, rec_bytes,
-               &ctl->full[stage]);
+      if (rec_bytes > 0) {
+        bulk_g2s(st + p.kg_off, p.rec_kg + item * p.tokens * 2 * kDk, rec_bytes,
+                 &ctl->full[stage]);
+        bulk_g2s(st + p.u_off, p.rec_u + item * p.tokens * kDk, rec_bytes,
+                 &ctl->full[stage]);
+      }
     } else {
       mbar_arrive(&ctl->full[stage]);
     }
@@ -155,9 +159,9 @@ __device__ void compute(const Params &p, uint8_t *smem, Ctrl *ctl, const Desc *d
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int g8 = tid >> 3, l8 = tid & 7;
-  float *kh = reinterpret_cast<float *>(smem + p.vec_off);  // [128] k_hat
-  float *dd = kh + kDk;                                        // [128] decay
-  float *ks = dd + kDk;                                        // [4] k square sums
+  float *kh = reinterpret_cast<float *>(smem + p.vec_off);  // [T][128] k_hat
+  float *dd = kh + KDA_MAX_TOKENS * kDk;                      // [T][128] decay
+  float *ks = dd + KDA_MAX_TOKENS * kDk;                      // [T][4] k square sums
   int cur_head = -1;
   float ea = 0.0f, dtb = 0.0f;
   for (int k = 0; k < n1 - n0; ++k) {
@@ -190,36 +194,53 @@ __device__ void compute(const Params &p, uint8_t *smem, Ctrl *ctl, const Desc *d
         for (int cc = 0; cc < 4; ++cc)
           S4[m][cc] = *reinterpret_cast<const float4 *>(page_s + (g8 + 32 * m) * kDk +
                                                         32 * cc + 4 * l8);
+      // k_hat (threads 0-127, channel c) and decay (threads 128-255, feature
+      // f) of every accepted token first, computed as the step kernel's front
+      // computes them (the k square sums by the same warp tree); then the
+      // token sweeps need no barrier (each thread's rows are its own).
+      float kv[KDA_MAX_TOKENS];
+      if (tid < 128) {
+        float sq[KDA_MAX_TOKENS];
+#pragma unroll
+        for (int t = 0; t < KDA_MAX_TOKENS; ++t) {
+          kv[t] = t < acc ? bf16_bits_to_float(kg[t * 2 * kDk + tid]) : 0.0f;
+          sq[t] = __fmul_rn(kv[t], kv[t]);
+        }
+        const float tot = warp_reduce_scatter<KDA_MAX_TOKENS>(sq, lane);
+        const int idx = lane >> 2;
+        if ((lane & 3) == 0 && idx < acc) ks[idx * 4 + warp] = tot;
+      } else {
+        const int f = tid - 128;
 #pragma unroll 1
-      for (int t = 0; t < acc; ++t) {
-        // k_hat (threads 0-127, channel c) and decay (threads 128-255, feature
-        // f), computed as the step kernel's front computes them.
-        float kv = 0.0f;
-        if (tid < 128) {
-          kv = bf16_bits_to_float(kg[t * 2 * kDk + tid]);
-          const float sq = warp_sum(__fmul_rn(kv, kv));
-          if (lane == 0) ks[warp] = sq;
-        } else {
-          const int f = tid - 128;
+        for (int t = 0; t < acc; ++t) {
           const float raw = bf16_bits_to_float(kg[t * 2 * kDk + kDk + f]);
           const float z = __fmul_rn(ea, __fadd_rn(raw, dtb));
-          dd[f] = exp_approx(__fmul_rn(p.lower_bound, sigmoid_approx(z)));
+          dd[t * kDk + f] = exp_approx(__fmul_rn(p.lower_bound, sigmoid_approx(z)));
         }
-        compute_sync();
-        if (tid < 128) {
-          const float kn = __fadd_rn(
-              __fadd_rn(__fadd_rn(ks[0], ks[2]), __fadd_rn(ks[1], ks[3])), 1.0e-6f);
-          kh[tid] = __fmul_rn(kv, rcp_approx(sqrt_approx(kn)));
+      }
+      compute_sync();
+      if (tid < 128) {
+#pragma unroll
+        for (int t = 0; t < KDA_MAX_TOKENS; ++t) {
+          if (t < acc) {
+            const float *k4s = ks + t * 4;
+            const float kn = __fadd_rn(
+                __fadd_rn(__fadd_rn(k4s[0], k4s[2]), __fadd_rn(k4s[1], k4s[3])), 1.0e-6f);
+            kh[t * kDk + tid] = __fmul_rn(kv[t], rcp_approx(sqrt_approx(kn)));
+          }
         }
-        compute_sync();
+      }
+      compute_sync();
+#pragma unroll 1
+      for (int t = 0; t < acc; ++t) {
         float U[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) U[m] = us[t * kDk + g8 + 32 * m];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const int key = 32 * cc + 4 * l8;
-          const float4 d4 = *reinterpret_cast<const float4 *>(dd + key);
-          const float4 k4 = *reinterpret_cast<const float4 *>(kh + key);
+          const float4 d4 = *reinterpret_cast<const float4 *>(dd + t * kDk + key);
+          const float4 k4 = *reinterpret_cast<const float4 *>(kh + t * kDk + key);
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             float2 lo = __fmul2_rn(make_float2(S4[m][cc].x, S4[m][cc].y),
@@ -232,7 +253,6 @@ __device__ void compute(const Params &p, uint8_t *smem, Ctrl *ctl, const Desc *d
             S4[m][cc] = make_float4(lo.x, lo.y, hi.x, hi.y);
           }
         }
-        compute_sync();  // kh / dd / ks are rewritten by the next token
       }
 #pragma unroll
       for (int m = 0; m < 4; ++m)
@@ -321,7 +341,7 @@ static int run(const kda_recover_args *a, cudaStream_t stream) {
   prm.bar_off = kStages * prm.stage_bytes;
   prm.desc_off = prm.bar_off + align_up(sizeof(Ctrl), 128);
   prm.vec_off = prm.desc_off + align_up(kStages * sizeof(Desc), 128);
-  const uint32_t total = prm.vec_off + (2 * kDk + 4) * 4;
+  const uint32_t total = prm.vec_off + (2 * KDA_MAX_TOKENS * kDk + 4 * KDA_MAX_TOKENS) * 4;
   if (total > static_cast<uint32_t>(di.max_smem)) return KDA_ERR_SHAPE;
   prm.src_slots = a->src_slots;
   prm.dst_slots = a->dst_slots;
