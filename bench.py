@@ -606,6 +606,27 @@ def main():
     achieved = nbytes["total"] / (kern_ms * 1e-3) / 1e9
     state_gbs = nbytes["state"] / (kern_ms * 1e-3) / 1e9
     traffic = ncu_traffic(w.name if rank == 0 else workload.name)
+    # Decode: the same pages moved with no arithmetic (kda_probe_page_copy, the
+    # step's two stages), timed after the step's region: the ceiling of this
+    # access pattern, beside the copy peak.
+    pattern = None
+    if T == 1:
+        from linear_attention_recurrent_kda_gb300.api import kda_probe_page_copy
+        pslots = d["slots"].view(-1).contiguous()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                kda_probe_page_copy(state=d["state"], slots=pslots, stream=stream)
+            p0 = torch.cuda.Event(enable_timing=True)
+            p1 = torch.cuda.Event(enable_timing=True)
+            p0.record(stream)
+            for _ in range(20):
+                kda_probe_page_copy(state=d["state"], slots=pslots, stream=stream)
+            p1.record(stream)
+        torch.cuda.synchronize(dev)
+        p_ms = p0.elapsed_time(p1) / 20
+        p_gbs = nbytes["state"] / (p_ms * 1e-3) / 1e9
+        pattern = {"ms": p_ms, "state_gbs": p_gbs, "frac": p_gbs / peak,
+                   "step_state_frac_of_pattern": state_gbs / p_gbs}
     # FP32 pipe: the recurrence's flop against the derived non-tensor FP32 peak
     # (SMs x 128 FP32 lanes x 2 flop per FMA x the maximum SM clock).
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -629,7 +650,7 @@ def main():
                      "algorithmic_bytes_per_launch": nbytes["total"],
                      "state_bytes_per_launch": nbytes["state"],
                      "state_gbs": state_gbs, "state_frac": state_gbs / peak,
-                     "kernel_ms": kern_ms},
+                     "kernel_ms": kern_ms, "access_pattern_ceiling": pattern},
         "fp32_pipe": {"achieved": fp32_tf, "peak": fp32_peak, "unit": "TFLOP/s",
                       "frac": fp32_tf / fp32_peak,
                       "flop_per_token_item": RECURRENCE_FLOP_PER_TOKEN_ITEM,
