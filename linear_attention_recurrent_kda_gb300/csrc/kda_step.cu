@@ -582,11 +582,12 @@ __device__ __forceinline__ void front_item(const Params &p, uint8_t *st,
   // sums combined as KdaWide.quad_sum does.
 #pragma unroll
   for (int t = 0; t < T; ++t) {
-    const float *s4 = ssum + t * 8;
+    const float4 sq4 = *reinterpret_cast<const float4 *>(ssum + t * 8);
+    const float4 sk4 = *reinterpret_cast<const float4 *>(ssum + t * 8 + 4);
     const float qn =
-        __fadd_rn(__fadd_rn(__fadd_rn(s4[0], s4[2]), __fadd_rn(s4[1], s4[3])), 1.0e-6f);
+        __fadd_rn(__fadd_rn(__fadd_rn(sq4.x, sq4.z), __fadd_rn(sq4.y, sq4.w)), 1.0e-6f);
     const float kn =
-        __fadd_rn(__fadd_rn(__fadd_rn(s4[4], s4[6]), __fadd_rn(s4[5], s4[7])), 1.0e-6f);
+        __fadd_rn(__fadd_rn(__fadd_rn(sk4.x, sk4.z), __fadd_rn(sk4.y, sk4.w)), 1.0e-6f);
     const float fq = rcp_approx(sqrt_approx(qn));
     const float fk = rcp_approx(sqrt_approx(kn));
     sv.q[t * kDk + c] = __fmul_rn(__fmul_rn(sv.q[t * kDk + c], fq), p.scale);
@@ -713,11 +714,16 @@ __device__ void front_role(const Params &p, uint8_t *smem, Ctrl *ctl,
 // Passes of the delta rule over the page held in registers (thread (g8, l8):
 // rows g8 + 32m, keys 32cc + 4l8 .. +3).  Each returns, per row m, this
 // thread's partial dot product (x and y halves of the packed accumulator
-// added last); a row's total is the 8-lane reduce_scatter8 of them.
+// added last); a row's total is the 8-lane reduce_scatter8 of them.  The k vector
+// travels in registers (kr): loaded once per token by the pass that first
+// needs it and reused by the next, which saves a quarter of the vector loads
+// from shared memory (the recurrence's shared-memory wavefronts, not its
+// FMAs, are what the record step's token loop competes for).
 
 // S *= d; partial rows of S k.
 __device__ __forceinline__ void pass_decay_dot(float4 (&S4)[4][4], const float *d,
-                                               const float *k, int l8, float (&part)[4]) {
+                                               const float *k, int l8, float (&part)[4],
+                                               float4 (&kr)[4]) {
   float2 acc[4];
 #pragma unroll
   for (int m = 0; m < 4; ++m) acc[m] = make_float2(0.0f, 0.0f);
@@ -726,6 +732,7 @@ __device__ __forceinline__ void pass_decay_dot(float4 (&S4)[4][4], const float *
     const int key = 32 * cc + 4 * l8;
     const float4 d4 = *reinterpret_cast<const float4 *>(d + key);
     const float4 k4 = *reinterpret_cast<const float4 *>(k + key);
+    kr[cc] = k4;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const float2 lo = __fmul2_rn(make_float2(S4[m][cc].x, S4[m][cc].y),
@@ -742,7 +749,7 @@ __device__ __forceinline__ void pass_decay_dot(float4 (&S4)[4][4], const float *
 }
 
 // S += k u (u of row m in U[m]); partial rows of S q.
-__device__ __forceinline__ void pass_update_dot(float4 (&S4)[4][4], const float *k,
+__device__ __forceinline__ void pass_update_dot(float4 (&S4)[4][4], const float4 (&kr)[4],
                                                 const float *q, const float (&U)[4],
                                                 int l8, float (&part)[4]) {
   float2 acc[4];
@@ -751,7 +758,7 @@ __device__ __forceinline__ void pass_update_dot(float4 (&S4)[4][4], const float 
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc) {
     const int key = 32 * cc + 4 * l8;
-    const float4 k4 = *reinterpret_cast<const float4 *>(k + key);
+    const float4 k4 = kr[cc];
     const float4 q4 = *reinterpret_cast<const float4 *>(q + key);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -775,7 +782,7 @@ __device__ __forceinline__ void pass_update_dot(float4 (&S4)[4][4], const float 
 // operations in the same order as pass_update_dot then pass_decay_dot, so the
 // results are identical; the two row reductions that follow are independent.
 __device__ __forceinline__ void pass_update_dot_decay_dot(
-    float4 (&S4)[4][4], const float *k, const float *q, const float (&U)[4],
+    float4 (&S4)[4][4], float4 (&kr)[4], const float *q, const float (&U)[4],
     const float *dn, const float *kn, int l8, float (&opart)[4], float (&dpart)[4]) {
   float2 oacc[4], dacc[4];
 #pragma unroll
@@ -786,10 +793,11 @@ __device__ __forceinline__ void pass_update_dot_decay_dot(
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc) {
     const int key = 32 * cc + 4 * l8;
-    const float4 k4 = *reinterpret_cast<const float4 *>(k + key);
+    const float4 k4 = kr[cc];
     const float4 q4 = *reinterpret_cast<const float4 *>(q + key);
     const float4 d4 = *reinterpret_cast<const float4 *>(dn + key);
     const float4 n4 = *reinterpret_cast<const float4 *>(kn + key);
+    kr[cc] = n4;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const float2 uu = make_float2(U[m], U[m]);
@@ -876,7 +884,8 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
       // No state is written between tokens: token t's update and output sweep
       // is fused with token t+1's decay and k-dot sweep (same arithmetic).
       float part[4];
-      pass_decay_dot(S4, sv.d, sv.k, l8, part);
+      float4 kr[4];
+      pass_decay_dot(S4, sv.d, sv.k, l8, part, kr);
       float u = __fmul_rn(
           __fsub_rn(bf16_bits_to_float(sv.v[my_row]), reduce_scatter8(part, l8)),
           sv.beta[0]);
@@ -887,11 +896,11 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
 #pragma unroll
         for (int m = 0; m < 4; ++m)
           U[m] = __shfl_sync(0xffffffffu, u, (lane & ~7) | (2 * m));
-        const float *kt = sv.k + t * kDk, *qt = sv.q + t * kDk;
+        const float *qt = sv.q + t * kDk;
         float opart[4];
         if (t + 1 < T) {
           float dpart[4];
-          pass_update_dot_decay_dot(S4, kt, qt, U, sv.d + (t + 1) * kDk,
+          pass_update_dot_decay_dot(S4, kr, qt, U, sv.d + (t + 1) * kDk,
                                     sv.k + (t + 1) * kDk, l8, opart, dpart);
           const float o = reduce_scatter8(opart, l8);
           const float dot = reduce_scatter8(dpart, l8);
@@ -900,7 +909,7 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
           u = __fmul_rn(__fsub_rn(bf16_bits_to_float(sv.v[(t + 1) * kDk + my_row]), dot),
                         sv.beta[t + 1]);
         } else {
-          pass_update_dot(S4, kt, qt, U, l8, opart);
+          pass_update_dot(S4, kr, qt, U, l8, opart);
           const float o = reduce_scatter8(opart, l8);
           if ((l8 & 1) == 0)
             sv.o[t * kDk + my_row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
@@ -911,7 +920,8 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
       for (int t = 0; t < T; ++t) {
         const float *kt = sv.k + t * kDk, *qt = sv.q + t * kDk;
         float part[4];
-        pass_decay_dot(S4, sv.d + t * kDk, kt, l8, part);
+        float4 kr[4];
+        pass_decay_dot(S4, sv.d + t * kDk, kt, l8, part, kr);
         const float dot = reduce_scatter8(part, l8);
         const float u = __fmul_rn(
             __fsub_rn(bf16_bits_to_float(sv.v[t * kDk + my_row]), dot), sv.beta[t]);
@@ -919,7 +929,7 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
 #pragma unroll
         for (int m = 0; m < 4; ++m)
           U[m] = __shfl_sync(0xffffffffu, u, (lane & ~7) | (2 * m));
-        pass_update_dot(S4, kt, qt, U, l8, part);
+        pass_update_dot(S4, kr, qt, U, l8, part);
         const float o = reduce_scatter8(part, l8);
         if ((l8 & 1) == 0)
           sv.o[t * kDk + my_row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
