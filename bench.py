@@ -355,32 +355,36 @@ def run_pattern(args):
     from linear_attention_recurrent_kda_gb300.api import kda_probe_page_copy
     from linear_attention_recurrent_kda_gb300.workloads import WORKLOADS, make_inputs
 
+    from linear_attention_recurrent_kda_gb300.accounting import step_bytes
     w = WORKLOADS[args.workload or "decode_b256_h32"]
-    if w.tokens != 1:                      # the probe follows decode's one page per item
+    if w.record:                           # record mode writes no page: nothing to probe
         w = WORKLOADS["decode_b256_h32"]
     host = make_inputs(w)
     dev = torch.device("cuda", 0)
     state, slots = host["state"].to(dev), host["slots"].to(dev)
-    live = int((host["slots"] > 0).sum()) * w.heads
-    nbytes = live * 2 * 128 * 128 * 4
+    accepted = host["accepted"].to(dev) if w.tokens > 1 else None
+    live = w.items if w.tokens > 1 else int((host["slots"] > 0).sum()) * w.heads
+    nbytes = step_bytes(w, host)["state"]
     stream = torch.cuda.Stream(device=dev)
     peak, peak_kind = measured_peak()
     res = {}
     for stages in (2, 3):
         with torch.cuda.stream(stream):
             for _ in range(args.warmup):
-                kda_probe_page_copy(state=state, slots=slots, stages=stages, stream=stream)
+                kda_probe_page_copy(state=state, slots=slots, accepted=accepted,
+                                    tokens=w.tokens, stages=stages, stream=stream)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for _ in range(args.steps):
-                kda_probe_page_copy(state=state, slots=slots, stages=stages, stream=stream)
+                kda_probe_page_copy(state=state, slots=slots, accepted=accepted,
+                                    tokens=w.tokens, stages=stages, stream=stream)
             e1.record(stream)
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1) / args.steps
         res[stages] = (ms, nbytes / (ms * 1e-3) / 1e9)
     ms2, gbs2 = res[2]
     line = {
-        "metric": "decode page access pattern (read + write back in place, no arithmetic)",
+        "metric": "step page access pattern (read, then every page write, no arithmetic)",
         "value": gbs2, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms2, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -606,21 +610,26 @@ def main():
     achieved = nbytes["total"] / (kern_ms * 1e-3) / 1e9
     state_gbs = nbytes["state"] / (kern_ms * 1e-3) / 1e9
     traffic = ncu_traffic(w.name if rank == 0 else workload.name)
-    # Decode: the same pages moved with no arithmetic (kda_probe_page_copy, the
-    # step's two stages), timed after the step's region: the ceiling of this
-    # access pattern, beside the copy peak.
+    # Decode and verify: the same pages moved with no arithmetic
+    # (kda_probe_page_copy, the step's two stages), timed after the step's
+    # region: the ceiling of this access pattern, beside the copy peak.
     pattern = None
-    if T == 1:
+    if not w.record:
         from linear_attention_recurrent_kda_gb300.api import kda_probe_page_copy
-        pslots = d["slots"].view(-1).contiguous()
+        pslots = d["slots"].view(-1).contiguous() if T == 1 else d["slots"]
+        pacc = d["accepted"] if T > 1 else None
+
+        def probe():
+            kda_probe_page_copy(state=d["state"], slots=pslots, accepted=pacc, tokens=T,
+                                stream=stream)
         with torch.cuda.stream(stream):
             for _ in range(3):
-                kda_probe_page_copy(state=d["state"], slots=pslots, stream=stream)
+                probe()
             p0 = torch.cuda.Event(enable_timing=True)
             p1 = torch.cuda.Event(enable_timing=True)
             p0.record(stream)
             for _ in range(20):
-                kda_probe_page_copy(state=d["state"], slots=pslots, stream=stream)
+                probe()
             p1.record(stream)
         torch.cuda.synchronize(dev)
         p_ms = p0.elapsed_time(p1) / 20

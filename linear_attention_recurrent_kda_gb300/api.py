@@ -251,22 +251,36 @@ def kda_oproj(*, partials, prefix, output, out_norm, blocks=None, norm=None,
         raise _lib.KdaError(rc, _lib.strerror(rc))
 
 
-def kda_probe_page_copy(*, state, slots, stages: int = 2, err=None,
-                        stream: Optional[torch.cuda.Stream] = None) -> None:
-    """Access-pattern probe (include/kda.h ``kda_probe_page_copy``): every
-    (request, head) page of ``state`` (float32 [num_slots, heads, 128, 128])
-    named by ``slots`` (int32 [batch]) is read into shared memory and written
-    back in place, with the decode step's schedule and no arithmetic."""
+def kda_probe_page_copy(*, state, slots, accepted=None, tokens: int = 1, stages: int = 2,
+                        err=None, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Access-pattern probe (include/kda.h ``kda_probe_page_copy``): the
+    step's page traffic with no arithmetic.  ``state`` float32 [num_slots,
+    heads, 128, 128]; decode (``tokens`` 1): ``slots`` int32 [batch], every
+    page read and written back in place; verify (``tokens`` T > 1):
+    ``slots`` int32 [batch, >= T] and ``accepted`` int32 [batch], the page
+    at slot ``slots[r, accepted[r]-1]`` written to each ``slots[r, t]``."""
     _check("state", state, torch.float32)
     if state.dim() != 4 or tuple(state.shape[2:]) != (128, 128):
         raise ValueError("state must be [num_slots, heads, 128, 128]")
     _check("slots", slots, torch.int32)
-    if slots.dim() != 1:
-        raise ValueError("slots must be [batch]")
+    T = int(tokens)
+    if T == 1:
+        if slots.dim() == 2 and slots.shape[1] == 1:
+            slots = slots.view(-1)
+        if slots.dim() != 1:
+            raise ValueError("slots must be [batch] for tokens == 1")
+        cols = 1
+    else:
+        if slots.dim() != 2 or slots.shape[1] < T:
+            raise ValueError("slots must be [batch, >= tokens]")
+        _check("accepted", accepted, torch.int32, (slots.shape[0],))
+        cols = slots.shape[1]
     a = _lib.KdaProbeArgs()
     a.batch, a.heads, a.num_slots, a.stages = (slots.shape[0], state.shape[1],
                                                state.shape[0], int(stages))
+    a.tokens, a.slot_cols = T, cols
     a.state, a.slots = _ptr(state), _ptr(slots)
+    a.accepted = _ptr(accepted) if T > 1 else None
     a.err = _ptr(err) if err is not None else None
     s = stream if stream is not None else torch.cuda.current_stream(state.device)
     rc = _lib.call("kda_probe_page_copy", a, s.cuda_stream)

@@ -1,14 +1,14 @@
-// Measurement probe: the HBM access pattern of the decode step without its
-// arithmetic (sm_103a).
+// Measurement probe: the HBM access pattern of the decode / verify step
+// without its arithmetic (sm_103a).
 //
-// Per (request, head) item, the 64 KiB FP32 state page at
-// state[slots[r], h] is read by one TMA bulk copy into a shared-memory stage
-// and written back to the same place by one bulk store: the bytes and the
-// order of the decode step (persistent CTAs, one per SM, over contiguous
-// item ranges, a ring of `stages` pages per CTA), with no conv, gate,
-// recurrence or epilogue.  Its bandwidth is the ceiling that the decode
-// step's own page traffic can reach on this memory system; the state pool is
-// unchanged by it.  One thread per CTA issues everything.
+// Per (request, head) item, the 64 KiB FP32 state page the step reads is
+// read by one TMA bulk copy into a shared-memory stage and written by bulk
+// stores to every page the step writes (decode: back in place; verify: the
+// slots of the T tokens): the bytes and the order of the step (persistent
+// CTAs, one per SM, over contiguous item ranges, a ring of `stages` pages per
+// CTA), with no conv, gate, recurrence or epilogue.  Its bandwidth is the
+// ceiling that the step's own page traffic can reach on this memory system.
+// One thread per CTA issues everything.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,69 +20,98 @@ namespace probe {
 
 constexpr uint32_t kPage = 128u * 128u * 4u;
 
+// An item's pages: the one it reads (src) and the ones it writes (dst; T of
+// them, the slots of its tokens, <= 0 skipped).  Live unless padded or out of
+// range (then flagged and skipped, as the step does).
+struct ProbeItem {
+  int src;
+  int dst[KDA_MAX_TOKENS];
+};
+
+__device__ __forceinline__ bool probe_resolve(const kda_probe_args &a, int n, ProbeItem &it) {
+  const int h = n / a.batch, r = n - h * a.batch;
+  (void)h;
+  const int T = a.tokens;
+  const int32_t *row = a.slots + static_cast<int64_t>(r) * a.slot_cols;
+  int off = 0;
+  if (T > 1) {
+    const int acc = __ldg(a.accepted + r);
+    if (acc < 1 || acc > T) {
+      if (a.err) atomicOr(a.err, KDA_DEVERR_ACCEPTED);
+      return false;
+    }
+    off = acc - 1;
+  }
+  it.src = __ldg(row + off);
+  if (it.src <= 0) return false;
+  bool bad = it.src >= a.num_slots;
+#pragma unroll
+  for (int t = 0; t < KDA_MAX_TOKENS; ++t) {
+    it.dst[t] = t < T ? (T > 1 ? __ldg(row + t) : it.src) : 0;
+    bad |= it.dst[t] >= a.num_slots;
+  }
+  if (bad && a.err) atomicOr(a.err, KDA_DEVERR_SLOT);
+  return !bad;
+}
+
 template <int S>
-__global__ void __launch_bounds__(32) page_copy_kernel(float *state, const int32_t *slots,
-                                                       int batch, int heads, int num_slots,
-                                                       int32_t *err) {
+__global__ void __launch_bounds__(32) page_copy_kernel(const __grid_constant__ kda_probe_args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full[S];
   __shared__ uint32_t abort_flag;
   if (threadIdx.x != 0) return;
-  const int items = batch * heads, G = gridDim.x;
+  const int items = a.batch * a.heads, G = gridDim.x;
   const int n0 = static_cast<int>(static_cast<int64_t>(items) * blockIdx.x / G);
   const int n1 = static_cast<int>(static_cast<int64_t>(items) * (blockIdx.x + 1) / G);
   abort_flag = 0u;
   for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  // Live items of the range, in order (slot <= 0: padding; slot beyond the
-  // pool: error flag, skipped).
-  auto next_live = [&](int n) -> int {
-    for (; n < n1; ++n) {
-      const int s = __ldg(slots + (n - (n / batch) * batch));
-      if (s >= num_slots) {
-        if (err) atomicOr(err, KDA_DEVERR_SLOT);
-      } else if (s > 0) {
-        break;
-      }
-    }
-    return n;
+  auto page = [&](int n, int slot) -> float * {
+    const int h = n / a.batch;
+    return a.state + (static_cast<int64_t>(slot) * a.heads + h) * (kPage / 4);
   };
-  auto page = [&](int n) -> float * {
-    const int h = n / batch, r = n - h * batch;
-    return state + (static_cast<int64_t>(__ldg(slots + r)) * heads + h) * (kPage / 4);
+  // The next live item at or after n (n1 when none), resolved into `it`.
+  auto next_live = [&](int n, ProbeItem &it) -> int {
+    for (; n < n1; ++n)
+      if (probe_resolve(a, n, it)) break;
+    return n;
   };
   const uint64_t pol = policy_evict_first();
   // The j-th live item of the range goes through stage j % S.
   int item[S];
+  ProbeItem res[S];
   int loaded = 0, n = n0;
   for (int s = 0; s < S; ++s) {
-    n = next_live(n);
+    n = next_live(n, res[s]);
     if (n >= n1) break;
     item[s] = n++;
     mbar_arrive_expect_tx(&full[s], kPage);
-    bulk_g2s(smem + s * kPage, page(item[s]), kPage, &full[s]);
+    bulk_g2s(smem + s * kPage, page(item[s], res[s].src), kPage, &full[s]);
     ++loaded;
   }
   for (int i = 0; i < loaded; ++i) {
     const int st = i % S;
     if (!mbar_wait(&full[st], static_cast<uint32_t>(i / S) & 1u, &abort_flag)) {
-      if (err) atomicOr(err, KDA_DEVERR_TIMEOUT);
+      if (a.err) atomicOr(a.err, KDA_DEVERR_TIMEOUT);
       uint32_t z = 0;  // bounded drain of the loads still in flight
       for (int q = i + 1; q < loaded; ++q)
         (void)mbar_wait(&full[q % S], static_cast<uint32_t>(q / S) & 1u, &z);
       break;
     }
-    bulk_s2g(page(item[st]), smem + st * kPage, kPage, pol);
+    // Every write of the item leaves from the staged page (one bulk group).
+    for (int t = 0; t < a.tokens; ++t)
+      if (res[st].dst[t] > 0)
+        bulk_s2g(page(item[st], res[st].dst[t]), smem + st * kPage, kPage, pol);
     bulk_commit();
     if (i >= 1) {
-      // Refill the stage of item i-1 once its store has read it.
+      // Refill the stage of item i-1 once its stores have read it.
       bulk_wait_read(1);
-      n = next_live(n);
+      const int ps = (i - 1) % S;
+      n = next_live(n, res[ps]);
       if (n < n1) {
-        const int ps = (i - 1) % S;
         item[ps] = n++;
         mbar_arrive_expect_tx(&full[ps], kPage);
-        bulk_g2s(smem + ps * kPage, page(item[ps]), kPage, &full[ps]);
+        bulk_g2s(smem + ps * kPage, page(item[ps], res[ps].src), kPage, &full[ps]);
         ++loaded;
       }
     }
@@ -95,8 +124,7 @@ static int launch(const kda_probe_args *a, int grid, cudaStream_t stream) {
   if (cudaFuncSetAttribute(page_copy_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            S * kPage) != cudaSuccess)
     return KDA_ERR_LAUNCH;
-  page_copy_kernel<S><<<grid, 32, S * kPage, stream>>>(
-      a->state, a->slots, a->batch, a->heads, a->num_slots, a->err);
+  page_copy_kernel<S><<<grid, 32, S * kPage, stream>>>(*a);
   return cudaGetLastError() == cudaSuccess ? KDA_SUCCESS : KDA_ERR_LAUNCH;
 }
 
@@ -104,11 +132,14 @@ static int run(const kda_probe_args *a, cudaStream_t stream) {
   if (!a) return KDA_ERR_NULL_ARGS;
   if (a->batch < 0 || a->heads < 0 || a->num_slots < 1 || a->stages < 2 || a->stages > 3)
     return KDA_ERR_SHAPE;
+  if (a->tokens < 1 || a->tokens > KDA_MAX_TOKENS) return KDA_ERR_TOKENS;
+  if (a->slot_cols < (a->tokens > 1 ? a->tokens : 1)) return KDA_ERR_SHAPE;
   if (static_cast<int64_t>(a->batch) * a->heads > (int64_t(1) << 30)) return KDA_ERR_SHAPE;
   if (a->batch == 0 || a->heads == 0) return KDA_SUCCESS;
-  if (!a->state || !a->slots) return KDA_ERR_NULL_POINTER;
+  if (!a->state || !a->slots || (a->tokens > 1 && !a->accepted)) return KDA_ERR_NULL_POINTER;
   if ((reinterpret_cast<uintptr_t>(a->state) & 15u) || (reinterpret_cast<uintptr_t>(a->slots) & 3u) ||
-      (a->err && (reinterpret_cast<uintptr_t>(a->err) & 3u)))
+      (a->err && (reinterpret_cast<uintptr_t>(a->err) & 3u)) ||
+      (a->tokens > 1 && (reinterpret_cast<uintptr_t>(a->accepted) & 3u)))
     return KDA_ERR_ALIGNMENT;
   int dev = 0, major = 0, minor = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||

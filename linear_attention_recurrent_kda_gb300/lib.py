@@ -85,6 +85,7 @@ class KdaProbeArgs(ctypes.Structure):
         ("batch", ctypes.c_int32), ("heads", ctypes.c_int32),
         ("num_slots", ctypes.c_int32), ("stages", ctypes.c_int32),
         ("state", _P), ("slots", _P), ("err", _P),
+        ("tokens", ctypes.c_int32), ("slot_cols", ctypes.c_int32), ("accepted", _P),
     ]
 
 

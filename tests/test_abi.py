@@ -33,7 +33,7 @@ def test_library_builds_and_exports_every_declared_symbol():
 
 
 def test_version_and_strerror():
-    assert kl.load().kda_abi_version() == 4
+    assert kl.load().kda_abi_version() == 5
     for code in range(0, 12):
         assert kl.strerror(code)
     assert "unknown" in kl.strerror(999)
@@ -127,6 +127,7 @@ def test_selftest_host_validation_without_gpu():
 def _pargs(**kw):
     a = kl.KdaProbeArgs()
     a.batch, a.heads, a.num_slots, a.stages = 4, 2, 8, 2
+    a.tokens, a.slot_cols = 1, 1
     a.state, a.slots = 1 << 20, 1 << 21
     for k, v in kw.items():
         setattr(a, k, v)
@@ -144,6 +145,12 @@ def _pargs(**kw):
     (dict(state=(1 << 20) + 4), kl.KDA_ERR_ALIGNMENT),
     (dict(slots=(1 << 21) + 2), kl.KDA_ERR_ALIGNMENT),
     (dict(err=(1 << 22) + 1), kl.KDA_ERR_ALIGNMENT),
+    (dict(tokens=0), kl.KDA_ERR_TOKENS),
+    (dict(tokens=9, slot_cols=9), kl.KDA_ERR_TOKENS),
+    (dict(slot_cols=0), kl.KDA_ERR_SHAPE),
+    (dict(tokens=4, slot_cols=3, accepted=1 << 23), kl.KDA_ERR_SHAPE),
+    (dict(tokens=4, slot_cols=4), kl.KDA_ERR_NULL_POINTER),
+    (dict(tokens=4, slot_cols=4, accepted=(1 << 23) + 2), kl.KDA_ERR_ALIGNMENT),
 ])
 def test_probe_host_validation_without_gpu(kw, code):
     assert kl.call("kda_probe_page_copy", _pargs(**kw), 0) == code

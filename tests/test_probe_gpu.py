@@ -1,7 +1,9 @@
-"""The access-pattern probe (kda_probe_page_copy) on the GPU: every live page
-is read and written back in place, so the pool is bit-identical afterwards;
-padding slots are skipped, slots beyond the pool raise KDA_DEVERR_SLOT and
-are skipped too."""
+"""The access-pattern probe (kda_probe_page_copy) on the GPU.  Decode: every
+live page is read and written back in place, so the pool is bit-identical
+afterwards; padding slots are skipped, slots beyond the pool raise
+KDA_DEVERR_SLOT and are skipped too.  Verify: each live item's read page
+(slot of token accepted-1) lands in the slots of all its tokens, and no
+other page changes."""
 from __future__ import annotations
 
 import pytest
@@ -45,3 +47,57 @@ def test_out_of_pool_slot_flags_and_skips():
     torch.cuda.synchronize()
     assert int(err.item()) == kl.KDA_DEVERR_SLOT
     assert torch.equal(_bits(state), _bits(before))
+
+
+@pytest.mark.parametrize("stages", [2, 3])
+@pytest.mark.parametrize("name", ["verify_q4_b128_h32", "verify_q8_record_b64_h64"])
+def test_verify_fanout(name, stages):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    slots, acc = inp["slots"], inp["accepted"]
+    if w.record:       # a verify-shaped table: distinct per-token slots for the live rows
+        B, T = slots.shape[0], w.tokens
+        slots = torch.zeros((B, T), dtype=torch.int32)
+        live = (inp["slots"][:, 0] > 0).nonzero().view(-1)
+        state_n = 1 + len(live) * T
+        for i, r in enumerate(live.tolist()):
+            slots[r] = torch.arange(1 + i * T, 1 + (i + 1) * T, dtype=torch.int32)
+        state = torch.randn((state_n, w.heads, 128, 128), generator=torch.Generator().manual_seed(5))
+    else:
+        state = inp["state"]
+    want = state.clone()
+    for r in range(slots.shape[0]):
+        src = int(slots[r, int(acc[r]) - 1])
+        if src <= 0:
+            continue
+        for t in range(w.tokens):
+            dst = int(slots[r, t])
+            if dst > 0:
+                want[dst] = state[src]
+    g = state.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda_probe_page_copy(state=g, slots=slots.cuda(), accepted=acc.cuda(), tokens=w.tokens,
+                        stages=stages, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(_bits(g.cpu()), _bits(want))
+
+
+def test_verify_errors_flag_and_skip():
+    w = WORKLOADS["verify_q4_b128_h32"]
+    inp = make_inputs(w)
+    slots, acc = inp["slots"].clone(), inp["accepted"].clone()
+    acc[3] = 0                      # accepted out of range
+    slots[5, 1] = w.num_slots       # a target beyond the pool
+    state = inp["state"]
+    g = state.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda_probe_page_copy(state=g, slots=slots.cuda(), accepted=acc.cuda(), tokens=w.tokens, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == kl.KDA_DEVERR_SLOT | kl.KDA_DEVERR_ACCEPTED
+    got = g.cpu()
+    for r in (3, 5):                # skipped items wrote nothing
+        for t in range(w.tokens):
+            s = int(slots[r, t])
+            if 0 < s < w.num_slots:
+                assert torch.equal(_bits(got[s]), _bits(state[s]))
