@@ -11,7 +11,7 @@ import torch
 
 from linear_attention_recurrent_kda_gb300 import lib as kl
 from linear_attention_recurrent_kda_gb300.api import kda_probe_page_copy
-from linear_attention_recurrent_kda_gb300.workloads import WORKLOADS, make_inputs
+from linear_attention_recurrent_kda_gb300.workloads import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -49,22 +49,19 @@ def test_out_of_pool_slot_flags_and_skips():
     assert torch.equal(_bits(state), _bits(before))
 
 
+VERIFY = {
+    "q4": WORKLOADS["verify_q4_b128_h32"],
+    "q8_ragged": Workload("probe_q8", batch=9, heads=4, tokens=8, num_slots=9 * 8 + 5,
+                          conv_width=10, slot_layout="verify", pad=2, seed=611),
+}
+
+
 @pytest.mark.parametrize("stages", [2, 3])
-@pytest.mark.parametrize("name", ["verify_q4_b128_h32", "verify_q8_record_b64_h64"])
+@pytest.mark.parametrize("name", sorted(VERIFY))
 def test_verify_fanout(name, stages):
-    w = WORKLOADS[name]
+    w = VERIFY[name]
     inp = make_inputs(w)
-    slots, acc = inp["slots"], inp["accepted"]
-    if w.record:       # a verify-shaped table: distinct per-token slots for the live rows
-        B, T = slots.shape[0], w.tokens
-        slots = torch.zeros((B, T), dtype=torch.int32)
-        live = (inp["slots"][:, 0] > 0).nonzero().view(-1)
-        state_n = 1 + len(live) * T
-        for i, r in enumerate(live.tolist()):
-            slots[r] = torch.arange(1 + i * T, 1 + (i + 1) * T, dtype=torch.int32)
-        state = torch.randn((state_n, w.heads, 128, 128), generator=torch.Generator().manual_seed(5))
-    else:
-        state = inp["state"]
+    slots, acc, state = inp["slots"], inp["accepted"], inp["state"]
     want = state.clone()
     for r in range(slots.shape[0]):
         src = int(slots[r, int(acc[r]) - 1])
