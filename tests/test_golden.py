@@ -15,9 +15,11 @@ import os
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
-from linear_attention_recurrent_kda_gb300.workloads import Workload, make_inputs
+from linear_attention_recurrent_kda_gb300.workloads import (OprojWorkload, Workload,
+                                                            make_oproj_inputs, make_inputs)
 from tests.hostdata import to_oracle
 
 SNAP = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
@@ -52,3 +54,21 @@ def test_oracle_matches_snapshot(case, mode):
     if w.record:
         assert _close(res["rec_u"].reshape(-1)[snap["rec_u"]["index"]], snap["rec_u"]["value"])
         assert res["rec_kg"].reshape(-1).view(np.uint16).tobytes().hex() == snap["rec_kg_hex"]
+
+
+def _obits(t):
+    return None if t is None else t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("mode", ["f32", "f64"])
+@pytest.mark.parametrize("case", range(len(DOC["oproj_cases"])))
+def test_oproj_oracle_matches_snapshot(case, mode):
+    c = DOC["oproj_cases"][case]
+    h = make_oproj_inputs(OprojWorkload(**c["workload"]))
+    res = oracle.oproj(partials=_obits(h["partials"]), prefix=_obits(h["prefix"]),
+                       out_norm=_obits(h["out_norm"]), blocks=_obits(h["blocks"]),
+                       norm=_obits(h["norm"]), query=_obits(h["query"]),
+                       has_delta=h["has_delta"], eps=h["eps"], out_eps=h["out_eps"], mode=mode)
+    assert res["output"].reshape(-1)[:16].tobytes().hex() == c[mode]["output_bf16_head_hex"]
+    assert hashlib.sha256(res["prefix"].tobytes()).hexdigest() == c[mode]["prefix_bf16_sha256"]
+    assert hashlib.sha256(res["output"].tobytes()).hexdigest() == c[mode]["output_bf16_sha256"]
