@@ -62,6 +62,7 @@ class _Args(ctypes.Structure):
         ("inter_out", _P), ("pre_out", _P), ("inter_in", _P), ("o_out", _P),
         ("err", _P), ("threads", ctypes.c_int32),
         ("conv_f32", ctypes.c_int32), ("conv_state_f32", _P),
+        ("silu_in_out", _P),
     ]
 
 
@@ -190,7 +191,8 @@ def run(inputs: Dict[str, object], *, mode: str = "f32",
     ``forced`` (uint16 [batch, heads, tokens, 4, dk]) replaces the oracle's own
     BF16 q, k, v and raw gates (teacher forcing).
     Returns output, state, conv_state, rec_u, rec_kg, err and, on request,
-    inter (BF16 intermediates), pre (their unrounded values) and o (the
+    inter (BF16 intermediates), pre (their unrounded values), silu_in (the
+    SiLU arguments of q, k, v: [batch, heads, tokens, 3, dk]) and o (the
     recurrence output before rounding).
     """
     if mode not in ("f32", "f64"):
@@ -222,6 +224,7 @@ def run(inputs: Dict[str, object], *, mode: str = "f32",
     inter = np.zeros((B, H, T, 4, D), dtype=u16) if want_intermediates else None
     pre = np.zeros((B, H, T, 4, D), dtype=np.float64) if want_intermediates else None
     o = np.zeros((B, H, T, D), dtype=np.float64) if want_intermediates else None
+    silu_in = np.zeros((B, H, T, 3, D), dtype=np.float64) if want_intermediates else None
     forced_c = _c(forced, u16) if forced is not None else None
     items_c = None if items is None else np.ascontiguousarray(items, dtype=i32)
     err = np.zeros(1, dtype=i32)
@@ -243,6 +246,7 @@ def run(inputs: Dict[str, object], *, mode: str = "f32",
     a.n_items = 0 if items_c is None else int(items_c.size)
     a.inter_out, a.pre_out, a.o_out = _ptr(inter), _ptr(pre), _ptr(o)
     a.inter_in = _ptr(forced_c)
+    a.silu_in_out = _ptr(silu_in)
     a.err = _ptr(err)
     a.threads = int(threads)
     fn = getattr(lib, f"kda_oracle_step_{mode}")
@@ -252,7 +256,7 @@ def run(inputs: Dict[str, object], *, mode: str = "f32",
     res = {"output": out, "state": state, "conv_state": conv_state,
            "rec_u": rec_u, "rec_kg": rec_kg, "err": int(err[0])}
     if want_intermediates:
-        res.update(inter=inter, pre=pre, o=o)
+        res.update(inter=inter, pre=pre, o=o, silu_in=silu_in)
     return res
 
 

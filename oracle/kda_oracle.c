@@ -101,6 +101,10 @@ typedef struct {
    * conv_state; taps are read as stored and the window is written as FP32. */
   int32_t conv_f32;
   float *conv_state_f32;
+  /* Test hook: double [batch,heads,tokens,3,dk], the SiLU argument (the
+   * convolution's FP32 sum) of q, k, v; the parity checks bound the error of
+   * an approximate SiLU by it.  NULL = unused. */
+  double *silu_in_out;
 } kda_oracle_args;
 
 /* ---- BF16 <-> binary floating point -------------------------------------- */
@@ -256,6 +260,7 @@ static int run_item(const kda_oracle_args *a, int r, int h) {
         for (int i = 0; i < 4; ++i) acc = R_FMA(win[t + i], wt[i], acc);
         real y = silu_unrounded(acc);
         const long ix = ((item * T + t) * 4 + p) * D + c;
+        if (a->silu_in_out) a->silu_in_out[((item * T + t) * 3 + p) * D + c] = (double)acc;
         if (a->pre_out) a->pre_out[ix] = (double)y;
         uint16_t yb = real_to_bf16(y);
         if (a->inter_out) a->inter_out[ix] = yb;

@@ -107,6 +107,11 @@ def test_conv_silu_against_sliding_window(tokens, has_bias):
                     np.testing.assert_allclose(got64, y, rtol=1e-13, atol=1e-15)
                     np.testing.assert_allclose(got32, y, rtol=8 * F32_EPS,
                                                atol=1e-30)
+                    # the SiLU argument the oracle reports is the conv sum
+                    np.testing.assert_allclose(r64["silu_in"][r, h, :, part, c], a,
+                                               rtol=1e-13, atol=1e-15)
+                    np.testing.assert_allclose(r32["silu_in"][r, h, :, part, c], a,
+                                               rtol=8 * F32_EPS, atol=1e-6)
 
 
 @pytest.mark.parametrize("tap", [0, 1, 2, 3])
