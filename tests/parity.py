@@ -10,11 +10,15 @@ So the comparison is anchored:
 Stage 1 (decision points): the GPU's BF16 q, k, v, raw_g (written through the
     library's ``dbg`` buffer by the same kernel) must equal the oracle's, or
     differ by exactly one BF16 ulp with the oracle's unrounded value within a
-    stated band of the midpoint between the two candidates:
-      q, k, v:  |y - mid| <= 2^-16 |y|              (SiLU through exp/divide)
+    band of the midpoint between the two candidates that the two sides'
+    arithmetic errors allow:
+      q, k, v:  |y - mid| <= silu_band(a) |y|, a = the SiLU argument (the
+                conv sum, bit-identical on both sides: same FMA chain);
+                silu_band is derived in its docstring from the error bounds of
+                the instructions the kernel uses
       raw_g:    each side a correct BF16 rounding of a value within
                 2 * 128 * 2^-24 * sum|products| of the exact float64 sum
-    and differences must stay rare (<= 1e-3 of the elements).
+    and differences must stay rare (at most ceil(1e-4 * elements)).
 Stage 2 (everything else): the oracle re-run with the GPU's BF16 values forced
     in (teacher forcing) must match the GPU:
       state pool        |gpu - ora| <= 1e-5 + 1e-4 |ora| on every element;
@@ -22,6 +26,12 @@ Stage 2 (everything else): the oracle re-run with the GPU's BF16 values forced
       output            within 2 BF16 ulp of max(|ora|, 2^-6) (outputs are
                         normalised to unit RMS); padded/error rows exactly +0;
       conv pool, rec_kg bit-exact;   rec_u  1e-5 + 1e-4 |ora|.
+Unanchored (reported, not a gate): the GPU against the oracle's own result,
+    with no forcing: BF16 flips, output ulps, state and rec_u error as a
+    fraction of the tolerance and the count of elements beyond it.  This needs
+    no ``dbg`` buffer, so it also covers launches without one (the
+    configuration a caller runs); ``same_bits`` checks such a launch against a
+    ``dbg`` launch of the same inputs bit for bit.
 """
 from __future__ import annotations
 
@@ -34,15 +44,31 @@ import oracle
 from linear_attention_recurrent_kda_gb300.api import step_from_inputs
 from tests.hostdata import bf16_bits_to_f64, bf16_ulp_diff, bits, to_oracle
 
-SILU_BAND = 2.0 ** -16
 GATE_BAND_ULPS = 2 * 128
-FLIP_RATE_MAX = 1e-3
+FLIP_RATE_MAX = 1e-4
 STATE_RTOL, STATE_ATOL = 1e-4, 1e-5
 OUT_ULPS = 2
 # The outputs are RMS-normalised (RMS ~ norm_weight * sigmoid(gate) <= 1.5);
 # an element far below that scale carries the absolute FP32 error of the
 # un-normalised recurrence output, so its ulps are counted at 2^-6.
 OUT_FLOOR = 2.0 ** -6
+
+
+def silu_band(a):
+    """Relative band around the oracle's unrounded SiLU value y = a/(1+e^-a)
+    inside which the kernel's value may fall on the other side of a BF16
+    midpoint.  Kernel: e = ex2.approx(fl(-a * fl(log2 e))) (relative error
+    <= 2^-22 for the instruction, plus |a| * 1.25 * 2^-24 from rounding the
+    argument and the constant), den = fl(1 + e), y = div.full(a, den)
+    (<= 2 ulp <= 2^-22).  Oracle: exp in double rounded once, then two
+    correctly rounded operations (<= 3 * 2^-24).  The error of e enters y
+    scaled by w = e / (1 + e).  First order, with one unit of slack:
+        |y_gpu - y_ora| <= |y| 2^-24 (8 + w (6 + 1.25 |a|))."""
+    a = np.asarray(a, np.float64)
+    with np.errstate(over="ignore"):
+        e = np.exp(-a)
+        w = np.where(np.isinf(e), 1.0, e / (1.0 + e))
+    return 2.0 ** -24 * (8.0 + w * (6.0 + 1.25 * np.abs(a)))
 
 
 def bf16_ulp_at(v):
@@ -132,7 +158,7 @@ def stage1(o, gpu_dbg, ora, items) -> Dict[str, int]:
 
     q, k, v: the SiLU inputs are bit-identical on both sides (same FMA chain),
     so a BF16 value may differ only by one ulp, at a midpoint the oracle's
-    unrounded value lies within SILU_BAND of.  raw_g: the FP32 gate sum has an
+    unrounded value lies within silu_band(a) of.  raw_g: the FP32 gate sum has an
     absolute error bound (2 * 128 * 2^-24 * sum|products|), which near zero can
     span several BF16 ulps, so each side's BF16 raw gate must be a correct
     rounding of some value within that bound of the exact (float64) sum."""
@@ -141,6 +167,7 @@ def stage1(o, gpu_dbg, ora, items) -> Dict[str, int]:
     g = gpu_dbg[rs, hs]                        # [n, T, 4, D]
     w = ora["inter"][rs, hs]
     pre = ora["pre"][rs, hs]
+    sin = ora["silu_in"][rs, hs]
     ulps = bf16_ulp_diff(g, w)
     qkv = ulps[:, :, :3]
     assert qkv.max(initial=0) <= 1, f"BF16 q/k/v differ by {qkv.max()} ulp"
@@ -150,9 +177,10 @@ def stage1(o, gpu_dbg, ora, items) -> Dict[str, int]:
         mid = 0.5 * (gv[n, t, part, c] + wv[n, t, part, c])
         counts["qkv"[part]] += 1
         y = pre[n, t, part, c]
-        assert abs(y - mid) <= SILU_BAND * abs(y), (
+        a = sin[n, t, part, c]
+        assert abs(y - mid) <= silu_band(a) * abs(y), (
             f"SiLU flip outside band: item {rs[n]*H+hs[n]} t{t} part{part} c{c} "
-            f"y={y!r} mid={mid!r}")
+            f"a={a!r} y={y!r} mid={mid!r} band={silu_band(a)!r}")
     # gate: exact sums of the sampled (item, token, feature) triples
     fa = bf16_bits_to_f64(o["f_a"])
     fb = bf16_bits_to_f64(o["f_b"]).reshape(H, D, -1)
@@ -174,7 +202,8 @@ def stage1(o, gpu_dbg, ora, items) -> Dict[str, int]:
     counts["g"] = int((ulps[:, :, 3] > 0).sum())
     flips = int((ulps > 0).sum())
     total = g.size
-    assert flips <= max(2, FLIP_RATE_MAX * total), f"{flips} flips of {total}"
+    assert flips <= int(np.ceil(FLIP_RATE_MAX * total)), f"{flips} flips of {total}"
+    counts["flips"] = flips
     counts["total"] = int(total)
     return counts
 
@@ -281,6 +310,69 @@ def compare(inputs: Dict[str, object], gpu: Dict[str, object],
     assert gpu["err"] == tf["err"], f"error word {gpu['err']} != {tf['err']}"
 
     # unanchored (reported, not a gate)
-    ud = bf16_ulp_diff(g_out, ora["output"][rr[:, None], cols])
-    stats["unanchored_out_max_ulp"] = int(ud.max(initial=0))
+    stats.update(unanchored(inputs, gpu, items=items, ora=ora, o=o))
     return stats
+
+
+def unanchored(inputs: Dict[str, object], gpu: Dict[str, object],
+               items: Optional[Sequence[int]] = None, ora=None, o=None) -> Dict[str, object]:
+    """The GPU result against the oracle's own (no teacher forcing): a report,
+    not a gate.  Needs no ``dbg`` buffer.  BF16 flips of the intermediates are
+    counted when the GPU result carries them; outputs in BF16 ulps; written
+    state pages and rec_u as the worst error over the anchored tolerance
+    1e-5 + 1e-4 |ora| and the number of elements beyond it (a flipped raw
+    gate moves its key's decay by up to about 1.5 %, so these can exceed the
+    tolerance without either side being wrong)."""
+    if o is None:
+        o = to_oracle(inputs)
+    H, T = o["heads"], o["tokens"]
+    sel = np.arange(o["batch"] * H) if items is None else np.asarray(items, np.int64)
+    if ora is None:
+        ora = oracle.run(o, mode="f32", items=None if items is None else sel,
+                         want_intermediates="dbg" in gpu)
+    rep: Dict[str, object] = {}
+    rs, hs = np.divmod(sel, H)
+    if "dbg" in gpu:
+        live = np.intersect1d(sel, live_items(o))
+        lr, lh = np.divmod(live, H)
+        fl = bf16_ulp_diff(gpu["dbg"][lr, lh], ora["inter"][lr, lh]) > 0
+        rep["unanchored_flips"] = {"qkv": int(fl[:, :, :3].sum()),
+                                   "g": int(fl[:, :, 3].sum()), "total": int(fl.size)}
+    rows = (rs[:, None] * T + np.arange(T)[None, :]).reshape(-1)
+    heads = np.repeat(hs, T)
+    cols = heads[:, None] * 128 + np.arange(128)[None, :]
+    ud = bf16_ulp_diff(gpu["output"][rows[:, None], cols], ora["output"][rows[:, None], cols])
+    rep["unanchored_out_max_ulp"] = int(ud.max(initial=0))
+    rep["unanchored_out_beyond_2ulp"] = int((ud > OUT_ULPS).sum())
+    worst, beyond, maxabs = 0.0, 0, 0.0
+    for (s, h) in sorted(written_pages(o, np.intersect1d(sel, live_items(o)))):
+        if s <= 0 or s >= o["num_slots"]:
+            continue
+        ref = ora["state"][s, h].astype(np.float64)
+        err = np.abs(gpu["state"][s, h].astype(np.float64) - ref)
+        lim = STATE_ATOL + STATE_RTOL * np.abs(ref)
+        worst = max(worst, float((err / lim).max()))
+        beyond += int((err > lim).sum())
+        maxabs = max(maxabs, float(err.max()))
+    rep["unanchored_state_worst_frac_of_tol"] = worst
+    rep["unanchored_state_beyond_tol"] = beyond
+    rep["unanchored_state_max_abs"] = maxabs
+    if o["record"]:
+        gu, tu = gpu["rec_u"][rs, hs].astype(np.float64), ora["rec_u"][rs, hs]
+        lim = STATE_ATOL + STATE_RTOL * np.abs(tu)
+        e = np.abs(gu - tu)
+        rep["unanchored_rec_u_worst_frac_of_tol"] = float((e / lim).max(initial=0.0))
+        rep["unanchored_rec_u_beyond_tol"] = int((e > lim).sum())
+    return rep
+
+
+def same_bits(a: Dict[str, object], b: Dict[str, object]) -> None:
+    """Two GPU results of the same inputs are identical bit for bit: outputs,
+    both pools, records and the error word (the ``dbg`` dump is compared only
+    when both carry it)."""
+    for key in ("output", "state", "conv_state", "rec_u", "rec_kg", "dbg"):
+        if key in a and key in b:
+            x, y = np.asarray(a[key]), np.asarray(b[key])
+            assert x.shape == y.shape and np.array_equal(x.view(np.uint8), y.view(np.uint8)), (
+                f"{key} differs between the two launches")
+    assert a["err"] == b["err"], f"error word {a['err']} != {b['err']}"

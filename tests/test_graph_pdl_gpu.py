@@ -1,10 +1,19 @@
-"""Chaining the KDA step: CUDA-graph replay and programmatic dependent launch.
+"""Chaining the KDA step: CUDA-graph replay and programmatic dependent launch,
+checked against the oracle.
 
-* A decode step captured once in a CUDA graph and replayed three times gives
-  the same pools and outputs, bit for bit, as three eager steps.
-* With use_pdl the kernel may start before the preceding kernel ends; its
-  producer waits (griddepcontrol) before reading the step inputs that kernel
-  writes, so a predecessor that writes x gives the same result as without PDL.
+* A step captured once in a CUDA graph and replayed: the first replay passes
+  the anchored comparison against the oracle on the inputs; the third replay
+  against the oracle run from the pools the second left; and three replays
+  equal three eager steps bit for bit.
+* With use_pdl the kernel may start before the preceding kernel ends.  Its
+  producer reads only the state pages, slots and accepted before waiting
+  (griddepcontrol) on that kernel; every other input is read, and every output
+  written, after the wait (KdaWide.kernel: the state rows first, then the
+  wait, then x, gate, f_a and beta).  So a predecessor that rewrites x, gate,
+  f_a, beta, the norm weight and the conv pool gives the oracle's result on
+  the new values; and a step whose gate input is the previous step's output
+  (two steps chained by PDL on disjoint pools, the first one triggering its
+  dependents early) gives the oracle's result on that output.
 """
 from __future__ import annotations
 
@@ -14,7 +23,8 @@ import torch
 
 from linear_attention_recurrent_kda_gb300.api import step_from_inputs
 from linear_attention_recurrent_kda_gb300.workloads import Workload, make_inputs
-from tests.parity import to_device
+from tests.hostdata import bits
+from tests.parity import compare, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -26,51 +36,102 @@ def wl(**kw):
     return Workload(**base)
 
 
-def snapshot(d, out):
-    torch.cuda.synchronize()
-    return [d["state"].clone(), d["conv_state"].clone(), out.clone()]
+class Launch:
+    """Device copies of a workload's inputs with output, dbg and error buffers,
+    and the prepared step over them."""
+
+    def __init__(self, inp, use_pdl=False, gate=None):
+        self.inp = inp
+        d = to_device(inp)
+        if gate is not None:
+            d["gate"] = gate
+        B, H, T = d["batch"], d["heads"], d["tokens"]
+        self.d = d
+        self.out = torch.full((B * T, H * 128), float("nan"), dtype=torch.bfloat16,
+                              device="cuda")
+        self.dbg = torch.zeros((B, H, T, 4, 128), dtype=torch.bfloat16, device="cuda")
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.step = step_from_inputs(d, self.out, err=self.err, dbg=self.dbg,
+                                     use_pdl=use_pdl)
+
+    def pools(self):
+        """Host copies of the current pools (inputs of a following step)."""
+        torch.cuda.synchronize()
+        return self.d["state"].cpu().clone(), self.d["conv_state"].cpu().clone()
+
+    def result(self):
+        torch.cuda.synchronize()
+        return {"output": bits(self.out), "state": self.d["state"].cpu().numpy(),
+                "conv_state": bits(self.d["conv_state"]), "err": int(self.err.item()),
+                "dbg": bits(self.dbg)}
+
+    def snapshot(self):
+        torch.cuda.synchronize()
+        return [self.d["state"].clone(), self.d["conv_state"].clone(), self.out.clone()]
 
 
 @pytest.mark.parametrize("tokens", [1, 3])
-def test_cuda_graph_replay_equals_eager(tokens):
+def test_cuda_graph_replay_matches_the_oracle(tokens):
     w = wl(tokens=tokens, slot_layout="decode" if tokens == 1 else "verify",
            conv_width=tokens + 2, num_slots=48 * tokens + 9)
     inp = make_inputs(w)
-    B, H = w.batch, w.heads
-    de, dg = to_device(inp), to_device(inp)
-    oe = torch.zeros((B * tokens, H * 128), dtype=torch.bfloat16, device="cuda")
-    og = torch.zeros_like(oe)
-    se = step_from_inputs(de, oe)
-    sg = step_from_inputs(dg, og)
+    eager, graphed = Launch(inp), Launch(inp)
     # one eager call on a throwaway copy configures the kernel before capture
-    dw = to_device(inp)
-    step_from_inputs(dw, torch.zeros_like(oe))()
+    Launch(inp).step()
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        sg()
+        graphed.step()
+    graph.replay()
+    compare(inp, graphed.result())
+    graph.replay()
+    mid = dict(inp)
+    mid["state"], mid["conv_state"] = graphed.pools()
+    graph.replay()
+    compare(mid, graphed.result())
     for _ in range(3):
-        se()
-        graph.replay()
-    a, b = snapshot(de, oe), snapshot(dg, og)
-    for x, y in zip(a, b):
+        eager.step()
+    for x, y in zip(eager.snapshot(), graphed.snapshot()):
         assert torch.equal(x, y)
 
 
-def test_pdl_after_a_kernel_that_writes_x():
-    w = wl()
+@pytest.mark.parametrize("tokens", [1, 4])
+def test_pdl_after_a_kernel_that_rewrites_the_inputs(tokens):
+    w = wl(tokens=tokens, slot_layout="decode" if tokens == 1 else "verify",
+           conv_width=tokens + 2, num_slots=48 * tokens + 9)
     inp = make_inputs(w)
-    B, H = w.batch, w.heads
-    x_new = torch.randn(inp["x"].shape, generator=torch.Generator().manual_seed(9))
-    x_new = x_new.to(torch.bfloat16).cuda()
-    outs = []
+    g = torch.Generator().manual_seed(9)
+    new = dict(inp)
+    for key in ("x", "gate", "f_a", "beta", "norm_weight"):
+        new[key] = torch.randn(inp[key].shape, generator=g).to(torch.bfloat16)
+    new["conv_state"] = torch.randn(inp["conv_state"].shape, generator=g).to(torch.bfloat16)
     for pdl in (False, True):
-        d = to_device(inp)
-        out = torch.zeros((B, H * 128), dtype=torch.bfloat16, device="cuda")
-        st = step_from_inputs(d, out, use_pdl=pdl)
+        L = Launch(inp, use_pdl=pdl)
+        staged = {k: new[k].cuda() for k in ("x", "gate", "f_a", "beta", "conv_state",
+                                             "norm_weight")}
         torch.cuda.synchronize()
-        torch.add(x_new, 0, out=d["x"])      # predecessor kernel writes x
-        st()
-        outs.append(snapshot(d, out))
-    for x, y in zip(*outs):
-        assert torch.equal(x, y)
+        # predecessor kernels rewrite the inputs the step reads after its wait
+        for k, v in staged.items():
+            L.d[k].copy_(v)
+        L.step()
+        compare(new, L.result())
+
+
+def test_two_steps_chained_by_pdl_on_disjoint_pools():
+    """Step B reads, as its output gate, the output step A writes; B is
+    launched with PDL right behind A (which triggers its dependents as soon
+    as its producers have issued their loads), so B's page loads overlap A
+    and B's gate read waits for A to finish."""
+    wa = wl(batch=64, heads=8, num_slots=80, pad=5, seed=331)
+    wb = wa.with_(seed=332)
+    ia, ib = make_inputs(wa), make_inputs(wb)
+    A = Launch(ia, use_pdl=True)
+    B = Launch(ib, use_pdl=True, gate=A.out)
+    torch.cuda.synchronize()
+    A.step()
+    B.step()
+    ra, rb = A.result(), B.result()
+    compare(ia, ra)
+    ib_seen = dict(ib)
+    ib_seen["gate"] = torch.from_numpy(ra["output"].view(np.int16)).view(torch.bfloat16)
+    compare(ib_seen, rb)

@@ -14,7 +14,7 @@ import oracle
 from linear_attention_recurrent_kda_gb300 import lib as kl
 from linear_attention_recurrent_kda_gb300.workloads import WORKLOADS, Workload, make_inputs
 from tests.hostdata import bits, to_oracle
-from tests.parity import compare, run_gpu, to_device
+from tests.parity import compare, run_gpu, same_bits, to_device, unanchored
 
 pytestmark = pytest.mark.gpu
 
@@ -51,6 +51,30 @@ def test_decode_ragged_tail_many_items_per_cta():
 
 def test_decode_many_items_per_cta_crosses_heads():
     check(small(batch=200, heads=5, num_slots=256, pad=17, seed=22))
+
+
+@pytest.mark.parametrize("tokens", [1, 3])
+def test_mostly_padding_balanced_ranges(tokens):
+    """Two thirds of the requests padded, live ones bunched at the end: each
+    CTA's range holds the same number of live items, padding rides along."""
+    lay = dict(slot_layout="decode") if tokens == 1 else dict(
+        slot_layout="verify", conv_width=tokens + 2)
+    w = small(tokens=tokens, batch=300, heads=4, num_slots=300 * tokens + 2, pad=200,
+              seed=280 + tokens, **lay)
+
+    def mutate(inp):
+        live = inp["slots"].reshape(300, -1)[:, 0] > 0 if tokens > 1 else inp["slots"] > 0
+        order = torch.argsort(live.to(torch.int8), stable=True)   # padding first
+        inp["slots"] = inp["slots"][order].contiguous()
+        if tokens > 1:
+            inp["accepted"] = inp["accepted"][order].contiguous()
+
+    check(w, mutate)
+
+
+def test_batch_beyond_the_balanced_scan():
+    """More requests than every CTA scans at start: equal item counts."""
+    check(small(batch=8200, heads=1, num_slots=8201, pad=8000, seed=290))
 
 
 def test_decode_all_padding():
@@ -215,18 +239,52 @@ def test_error_items_flag_and_pad():
 
 # --------------------------------------------------- the five named workloads
 
+@pytest.mark.parametrize("path", [kl.KDA_PATH_AUTO, kl.KDA_PATH_SPLIT])
 @pytest.mark.parametrize("name", ["decode_b256_h32", "verify_q4_b128_h32",
                                   "verify_q8_record_b64_h64"])
-def test_full_size_workloads_sampled(name):
-    """Full-size launch (the benchmark's configuration); the oracle checks a
-    seeded sample of items one by one, plus every padded item."""
+def test_full_size_workloads_sampled(name, path):
+    """Full-size launch as a caller makes it (no dbg buffer; the automatic
+    path is the one the benchmark times): its pools, outputs, records and
+    error word equal, bit for bit, those of a launch with the dbg buffer on
+    the same inputs, which the anchored comparison checks against the oracle
+    on a seeded sample of items one by one (plus every padded item); the
+    product launch itself is also compared with the oracle unanchored."""
     w = WORKLOADS[name]
     inp = make_inputs(w)
-    gpu = run_gpu(inp)
     rng = np.random.default_rng(5)
     items = np.sort(rng.choice(w.items, size=96, replace=False))
-    st = compare(inp, gpu, items=items)
-    print(name, st)
+    prod = run_gpu(inp, dbg=False, path=path)
+    rep = unanchored(inp, prod, items=items)
+    checked = run_gpu(inp, dbg=True, path=path)
+    same_bits(prod, checked)
+    del prod
+    st = compare(inp, checked, items=items)
+    print(name, path, st, rep)
+
+
+PRODUCT_CASES = {
+    "decode_pad": dict(batch=37, heads=9, pad=5, seed=21),
+    "decode_gm1_bias": dict(batch=40, heads=6, gate_mode=1, has_bias=True, seed=60),
+    "verify4_skips": dict(tokens=4, slot_layout="verify", conv_width=7, batch=23,
+                          heads=7, num_slots=23 * 4 + 5, pad=3, seed=34),
+    "record8_gm1_bias": dict(tokens=8, slot_layout="checkpoint", conv_width=10,
+                             record=True, gate_mode=1, has_bias=True, batch=19,
+                             heads=6, num_slots=25, pad=2, seed=58),
+}
+
+
+@pytest.mark.parametrize("path", [kl.KDA_PATH_PERSISTENT, kl.KDA_PATH_SPLIT])
+@pytest.mark.parametrize("case", list(PRODUCT_CASES))
+def test_launch_without_dbg_is_the_checked_launch(case, path):
+    """Every item compared: a launch without the dbg buffer gives the bits of
+    the dbg launch, which passes the anchored comparison."""
+    w = small(**PRODUCT_CASES[case])
+    inp = make_inputs(w)
+    prod = run_gpu(inp, dbg=False, path=path)
+    checked = run_gpu(inp, dbg=True, path=path)
+    same_bits(prod, checked)
+    st = compare(inp, checked)
+    print(case, path, st)
 
 
 # ------------------------------------------------------------ host errors
