@@ -35,8 +35,10 @@
  * Ownership and threading: the caller owns every buffer; every pointer is a
  * DEVICE pointer of the current device.  The library allocates nothing,
  * never synchronises, and enqueues exactly one kernel on `stream` per call.
- * Calls are reentrant; two calls that write the same pool regions must be
- * ordered by the caller (same stream or events).
+ * Calls are reentrant and may come from several host threads at once (the
+ * first call on a device reads its attributes and configures the kernel
+ * under a lock); two calls that write the same pool regions must be ordered
+ * by the caller (same stream or events).
  *
  * Aliasing contract: within one call, the state pages and conv rows touched
  * by different requests must be distinct (distinct slots per request).  An
@@ -97,9 +99,17 @@ typedef struct kda_args {
                        /* over rank quarters, then 0 + (((c0+c1)+c2)+c3)     */
   int32_t has_bias;    /* conv bias present                                  */
   int32_t record;      /* record ("RecoverSSM verify") mode, T > 1 only      */
-  int32_t use_pdl;     /* launch with programmatic dependent launch; the     */
-                       /* state/conv pools, slots and accepted are then read */
-                       /* before the preceding kernel finishes               */
+  int32_t use_pdl;     /* launch with programmatic dependent launch (the     */
+                       /* page's griddepcontrol ordering): the kernel may    */
+                       /* start before the preceding kernel on the stream    */
+                       /* ends.  It reads the state pages, slots and         */
+                       /* accepted BEFORE waiting for that kernel; every     */
+                       /* other input (x, gate, f_a, beta, the conv pool,    */
+                       /* the weights) and all of its writes come after.  So */
+                       /* the preceding kernel must not write the state      */
+                       /* pool, slots or accepted: two steps chained with    */
+                       /* PDL must use disjoint state pages.  Ignored by the */
+                       /* cluster-split path (path 2).                       */
 
   const void *x;            /* bf16 [B*T, 3*dim]  q | k | v column blocks    */
   const void *conv_weight;  /* bf16 [3, 4, dim]   (part, tap, channel)       */
@@ -225,38 +235,6 @@ typedef struct kda_oproj_args {
  * outside the ranges above), KDA_ERR_ALIGNMENT, KDA_ERR_DEVICE,
  * KDA_ERR_LAUNCH; nothing is launched on error.  One kernel on `stream`. */
 int kda_oproj(const kda_oproj_args *args, void *stream);
-
-/* Measurement probe: the step's HBM page traffic without its arithmetic.
- * For every (request r, head h) item (item n = h * batch + r, the step's
- * order) the 64 KiB FP32 page the step reads is read into shared memory by
- * one TMA bulk copy and written by bulk stores to every page the step
- * writes: tokens == 1 (decode) reads state[slots[r], h] and writes it back
- * in place; tokens T > 1 (verify) reads state[slots[r, accepted[r]-1], h]
- * and writes it to state[slots[r, t], h] for each t < T whose slot is > 0.
- * One CTA per SM over contiguous item ranges with a ring of `stages` (2 or
- * 3) pages, as the step schedules its pages.  Decode leaves the pool's
- * values unchanged.  Its bandwidth bounds what the step's page traffic can
- * reach.
- *   state     float [num_slots, heads, 128, 128], 16-byte aligned, in/out
- *   slots     int32 [batch, slot_cols] (device); a read slot <= 0 skips the
- *             item; any slot >= num_slots skips it and sets KDA_DEVERR_SLOT
- *   accepted  int32 [batch] (device, tokens > 1); outside 1..T skips the
- *             item and sets KDA_DEVERR_ACCEPTED
- *   err       optional device word (4-byte aligned) for KDA_DEVERR_* flags
- * Errors: KDA_ERR_NULL_ARGS, KDA_ERR_TOKENS (tokens outside 1..8),
- * KDA_ERR_SHAPE (negative sizes, num_slots < 1, stages outside 2..3,
- * slot_cols < 1, or slot_cols < tokens when tokens > 1),
- * KDA_ERR_NULL_POINTER, KDA_ERR_ALIGNMENT, KDA_ERR_DEVICE, KDA_ERR_LAUNCH;
- * nothing is launched on error.  One kernel on `stream`. */
-typedef struct kda_probe_args {
-  int32_t batch, heads, num_slots, stages;
-  float *state;
-  const int32_t *slots;
-  int32_t *err;
-  int32_t tokens, slot_cols;  /* 1 and 1 for decode                         */
-  const int32_t *accepted;    /* tokens > 1 only                             */
-} kda_probe_args;
-int kda_probe_page_copy(const kda_probe_args *args, void *stream);
 
 /* Self-test of the bounded on-chip waits that every kernel above uses: one
  * CTA waits on an mbarrier that nothing completes; the wait gives up after

@@ -42,6 +42,14 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _same_device(dev, **tensors):
+    """Every given tensor (None skipped) lives on ``dev``: the kernel would
+    otherwise dereference another GPU's pointer."""
+    for name, t in tensors.items():
+        if t is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, expected {dev}")
+
+
 class KdaStep:
     """A prepared KDA step over fixed device tensors.
 
@@ -103,10 +111,12 @@ class KdaStep:
         _check("err", err, i32, allow_none=True)
         _check("dbg", dbg, bf, (B, H, T, 4, DK), allow_none=True)
         dev = output.device
-        for name, t in (("x", x), ("state", state), ("conv_state", conv_state),
-                        ("slots", slots), ("f_b", f_b)):
-            if t.device != dev:
-                raise ValueError(f"{name} is on {t.device}, output on {dev}")
+        _same_device(dev, x=x, conv_weight=conv_weight, conv_bias=conv_bias,
+                     conv_state=conv_state, f_a=f_a, f_b=f_b, beta=beta, a_log=a_log,
+                     dt_bias=dt_bias, slots=slots, state=state, gate=gate,
+                     norm_weight=norm_weight, accepted=accepted if T > 1 else None,
+                     rec_u=rec_u if record else None, rec_kg=rec_kg if record else None,
+                     err=err, dbg=dbg)
 
         a = _lib.KdaArgs()
         a.batch, a.heads, a.tokens = B, H, T
@@ -133,8 +143,10 @@ class KdaStep:
                       conv_bias, rec_u, rec_kg, err, dbg)
 
     def __call__(self, stream: Optional[torch.cuda.Stream] = None) -> None:
-        s = stream if stream is not None else torch.cuda.current_stream(self.device)
-        rc = _lib.call(self.entry, self.args, s.cuda_stream)
+        # the library launches on the current device: make it the tensors' one
+        with torch.cuda.device(self.device):
+            s = stream if stream is not None else torch.cuda.current_stream(self.device)
+            rc = _lib.call(self.entry, self.args, s.cuda_stream)
         if rc != _lib.KDA_SUCCESS:
             raise _lib.KdaError(rc, _lib.strerror(rc))
 
@@ -196,6 +208,8 @@ def kda_recover(*, state, src_slots, dst_slots, accepted, rec_u, rec_kg, a_log,
     _check("a_log", a_log, f32, (H,))
     _check("dt_bias", dt_bias, f32, (H * DK,))
     _check("err", err, i32, allow_none=True)
+    _same_device(state.device, src_slots=src_slots, dst_slots=dst_slots, accepted=accepted,
+                 rec_u=rec_u, rec_kg=rec_kg, a_log=a_log, dt_bias=dt_bias, err=err)
     a = _lib.KdaRecoverArgs()
     a.batch, a.heads, a.tokens, a.num_slots = B, H, T, state.shape[0]
     a.src_slots, a.dst_slots, a.accepted = (_ptr(src_slots), _ptr(dst_slots),
@@ -204,8 +218,9 @@ def kda_recover(*, state, src_slots, dst_slots, accepted, rec_u, rec_kg, a_log,
     a.a_log, a.dt_bias = _ptr(a_log), _ptr(dt_bias)
     a.lower_bound = float(lower_bound)
     a.state, a.err = _ptr(state), _ptr(err)
-    s = stream if stream is not None else torch.cuda.current_stream(state.device)
-    rc = _lib.call("kda_recover", a, s.cuda_stream)
+    with torch.cuda.device(state.device):
+        s = stream if stream is not None else torch.cuda.current_stream(state.device)
+        rc = _lib.call("kda_recover", a, s.cuda_stream)
     if rc != _lib.KDA_SUCCESS:
         raise _lib.KdaError(rc, _lib.strerror(rc))
 
@@ -236,6 +251,9 @@ def kda_oproj(*, partials, prefix, output, out_norm, blocks=None, norm=None,
         nb = blocks.shape[1]
         _check("norm", norm, bf, (D,))
         _check("query", query, bf, (D,))
+    _same_device(partials.device, prefix=prefix, output=output, out_norm=out_norm,
+                 blocks=blocks if nb else None, norm=norm if nb else None,
+                 query=query if nb else None)
     a = _lib.KdaOprojArgs()
     a.tp, a.tokens, a.hidden, a.nb = tp, T, D, nb
     a.has_delta = int(bool(has_delta))
@@ -245,44 +263,8 @@ def kda_oproj(*, partials, prefix, output, out_norm, blocks=None, norm=None,
     a.norm = _ptr(norm) if nb else None
     a.query = _ptr(query) if nb else None
     a.eps, a.out_eps = float(eps), float(out_eps)
-    s = stream if stream is not None else torch.cuda.current_stream(partials.device)
-    rc = _lib.call("kda_oproj", a, s.cuda_stream)
-    if rc != _lib.KDA_SUCCESS:
-        raise _lib.KdaError(rc, _lib.strerror(rc))
-
-
-def kda_probe_page_copy(*, state, slots, accepted=None, tokens: int = 1, stages: int = 2,
-                        err=None, stream: Optional[torch.cuda.Stream] = None) -> None:
-    """Access-pattern probe (include/kda.h ``kda_probe_page_copy``): the
-    step's page traffic with no arithmetic.  ``state`` float32 [num_slots,
-    heads, 128, 128]; decode (``tokens`` 1): ``slots`` int32 [batch], every
-    page read and written back in place; verify (``tokens`` T > 1):
-    ``slots`` int32 [batch, >= T] and ``accepted`` int32 [batch], the page
-    at slot ``slots[r, accepted[r]-1]`` written to each ``slots[r, t]``."""
-    _check("state", state, torch.float32)
-    if state.dim() != 4 or tuple(state.shape[2:]) != (128, 128):
-        raise ValueError("state must be [num_slots, heads, 128, 128]")
-    _check("slots", slots, torch.int32)
-    T = int(tokens)
-    if T == 1:
-        if slots.dim() == 2 and slots.shape[1] == 1:
-            slots = slots.view(-1)
-        if slots.dim() != 1:
-            raise ValueError("slots must be [batch] for tokens == 1")
-        cols = 1
-    else:
-        if slots.dim() != 2 or slots.shape[1] < T:
-            raise ValueError("slots must be [batch, >= tokens]")
-        _check("accepted", accepted, torch.int32, (slots.shape[0],))
-        cols = slots.shape[1]
-    a = _lib.KdaProbeArgs()
-    a.batch, a.heads, a.num_slots, a.stages = (slots.shape[0], state.shape[1],
-                                               state.shape[0], int(stages))
-    a.tokens, a.slot_cols = T, cols
-    a.state, a.slots = _ptr(state), _ptr(slots)
-    a.accepted = _ptr(accepted) if T > 1 else None
-    a.err = _ptr(err) if err is not None else None
-    s = stream if stream is not None else torch.cuda.current_stream(state.device)
-    rc = _lib.call("kda_probe_page_copy", a, s.cuda_stream)
+    with torch.cuda.device(partials.device):
+        s = stream if stream is not None else torch.cuda.current_stream(partials.device)
+        rc = _lib.call("kda_oproj", a, s.cuda_stream)
     if rc != _lib.KDA_SUCCESS:
         raise _lib.KdaError(rc, _lib.strerror(rc))

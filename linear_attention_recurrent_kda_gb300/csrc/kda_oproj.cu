@@ -29,6 +29,7 @@
 
 #include "../../include/kda.h"
 #include "kda_device.cuh"
+#include "kda_host.h"
 
 namespace kda {
 namespace oproj {
@@ -274,12 +275,9 @@ static int run(const kda_oproj_args *a, cudaStream_t stream) {
       !aligned16(a->output) ||
       (a->nb > 0 && (!aligned16(a->blocks) || !aligned16(a->norm) || !aligned16(a->query))))
     return KDA_ERR_ALIGNMENT;
-  int dev = 0, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return KDA_ERR_DEVICE;
-  if (major != 10 || minor != 3) return KDA_ERR_DEVICE;
+  int dev = 0;
+  DeviceFacts df;
+  if (!current_device(&dev, &df)) return KDA_ERR_DEVICE;
 
   Params prm;
   prm.tp = a->tp;

@@ -27,6 +27,7 @@
 
 #include "../../include/kda.h"
 #include "kda_device.cuh"
+#include "kda_host.h"
 
 namespace kda {
 namespace recover {
@@ -291,12 +292,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_recover_kernel(const __grid_c
 
 static uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-struct DeviceInfo {
-  int sms = 0, max_smem = 0;
-  bool ok = false, configured = false;
-};
-static DeviceInfo g_dev[64];
-
 static int run(const kda_recover_args *a, cudaStream_t stream) {
   if (!a) return KDA_ERR_NULL_ARGS;
   if (a->tokens < 1 || a->tokens > KDA_MAX_TOKENS) return KDA_ERR_TOKENS;
@@ -315,19 +310,8 @@ static int run(const kda_recover_args *a, cudaStream_t stream) {
       !al(a->a_log, 4) || !al(a->dt_bias, 4) || (a->err && !al(a->err, 4)))
     return KDA_ERR_ALIGNMENT;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KDA_ERR_DEVICE;
-  DeviceInfo &di = g_dev[dev];
-  if (!di.ok) {
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&di.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-            cudaSuccess)
-      return KDA_ERR_DEVICE;
-    if (major != 10 || minor != 3) return KDA_ERR_DEVICE;
-    di.ok = true;
-  }
+  DeviceFacts df;
+  if (!current_device(&dev, &df)) return KDA_ERR_DEVICE;
   const int T = a->tokens;
   Params prm;
   prm.batch = a->batch;
@@ -342,7 +326,7 @@ static int run(const kda_recover_args *a, cudaStream_t stream) {
   prm.desc_off = prm.bar_off + align_up(sizeof(Ctrl), 128);
   prm.vec_off = prm.desc_off + align_up(kStages * sizeof(Desc), 128);
   const uint32_t total = prm.vec_off + (2 * KDA_MAX_TOKENS * kDk + 4 * KDA_MAX_TOKENS) * 4;
-  if (total > static_cast<uint32_t>(di.max_smem)) return KDA_ERR_SHAPE;
+  if (total > static_cast<uint32_t>(df.max_smem)) return KDA_ERR_SHAPE;
   prm.src_slots = a->src_slots;
   prm.dst_slots = a->dst_slots;
   prm.accepted = a->accepted;
@@ -353,13 +337,11 @@ static int run(const kda_recover_args *a, cudaStream_t stream) {
   prm.lower_bound = a->lower_bound;
   prm.state = a->state;
   prm.err = a->err;
-  if (!di.configured) {
-    if (cudaFuncSetAttribute(kda_recover_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             di.max_smem) != cudaSuccess)
-      return KDA_ERR_LAUNCH;
-    di.configured = true;
-  }
-  const int grid = prm.items < di.sms ? prm.items : di.sms;
+  static std::atomic<bool> configured[kMaxDevices];
+  if (!set_smem_limit_once(configured, dev, reinterpret_cast<const void *>(kda_recover_kernel),
+                           df.max_smem))
+    return KDA_ERR_LAUNCH;
+  const int grid = prm.items < df.sms ? prm.items : df.sms;
   kda_recover_kernel<<<grid, kThreads, total, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? KDA_SUCCESS : KDA_ERR_LAUNCH;
 }

@@ -51,6 +51,7 @@
 
 #include "../../include/kda.h"
 #include "kda_device.cuh"
+#include "kda_host.h"
 
 namespace kda {
 
@@ -252,11 +253,12 @@ __device__ void producer_role(const Params &p, uint8_t *smem, Ctrl *ctl,
   bool aborted = false;
 
   // Prologue: the first pages go out before waiting on the preceding kernel
-  // (state pool, slots and accepted are not its outputs).
+  // (the state pool, slots and accepted must not be its outputs); nothing is
+  // written and no other input is read before the wait.
+  int pro_flags = 0;
   for (int k = 0; k < pro; ++k) {
     ItemDesc &d = desc[k];
-    const int flags = resolve_item<T, RECORD>(p, n0 + k, d);
-    if (flags && p.err) atomicOr(p.err, flags);
+    pro_flags |= resolve_item<T, RECORD>(p, n0 + k, d);
     if (d.status == kLive) {
       mbar_expect_tx(&ctl->full[k], kPageBytes);
       issue_page(p, smem + static_cast<size_t>(k) * p.stage_bytes, n0 + k, d,
@@ -264,6 +266,7 @@ __device__ void producer_role(const Params &p, uint8_t *smem, Ctrl *ctl,
     }
   }
   griddep_wait();
+  if (pro_flags && p.err) atomicOr(p.err, pro_flags);
   for (int k = 0; k < pro; ++k) {
     ItemDesc &d = desc[k];
     load_beta<T>(p, n0 + k, d);
@@ -651,8 +654,7 @@ __device__ void front_role(const Params &p, uint8_t *smem, Ctrl *ctl,
   const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
   float *ssum = reinterpret_cast<float *>(smem + p.scratch_off);   // [T][2][4]
   float *osum = reinterpret_cast<float *>(smem + p.rscratch_off);  // [T][4]
-  const float nw = bf16_bits_to_float(
-      __ldg(reinterpret_cast<const uint16_t *>(p.norm_weight) + c));
+  float nw = 0.0f;  // norm weight of channel c, read after the first stage lands
   bool aborted = false;
   FrontConst fc;
   int cur_head = -1;
@@ -665,6 +667,11 @@ __device__ void front_role(const Params &p, uint8_t *smem, Ctrl *ctl,
       aborted = true;
       break;
     }
+    // A landed stage means the producer has passed its wait on the preceding
+    // kernel (programmatic dependent launch): inputs other than the state
+    // pool, slots and accepted may be read from here on.
+    if (k == 0)
+      nw = bf16_bits_to_float(__ldg(reinterpret_cast<const uint16_t *>(p.norm_weight) + c));
     const int n = n0 + k;
     const int h = n / p.batch;
     const ItemDesc &dsc = desc[stage];
@@ -1130,25 +1137,14 @@ static bool make_layout(int T, int W, bool record, bool conv_f32, int max_smem,
   return false;
 }
 
-struct DeviceInfo {
-  int sms = 0;
-  int max_smem = 0;
-  bool ok = false;
-  bool configured[KDA_MAX_TOKENS + 1][2] = {};
-};
-
-static DeviceInfo g_dev[64];
-
 template <int T, bool RECORD>
-static int launch_t(const Params &prm, const Layout &L, DeviceInfo &di, int grid,
-                    int use_pdl, cudaStream_t stream) {
+static int launch_t(const Params &prm, const Layout &L, int dev, const DeviceFacts &df,
+                    int grid, int use_pdl, cudaStream_t stream) {
   auto kern = kda_step_kernel<T, RECORD>;
-  if (!di.configured[T][RECORD]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             di.max_smem) != cudaSuccess)
-      return KDA_ERR_LAUNCH;
-    di.configured[T][RECORD] = true;
-  }
+  static std::atomic<bool> configured[kMaxDevices];
+  if (!set_smem_limit_once(configured, dev, reinterpret_cast<const void *>(kern),
+                           df.max_smem))
+    return KDA_ERR_LAUNCH;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -1203,24 +1199,10 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
     return KDA_ERR_ALIGNMENT;
 
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KDA_ERR_DEVICE;
-  DeviceInfo &di = g_dev[dev];
-  if (!di.ok) {
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) !=
-            cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) !=
-            cudaSuccess ||
-        cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) !=
-            cudaSuccess ||
-        cudaDeviceGetAttribute(&di.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin,
-                               dev) != cudaSuccess)
-      return KDA_ERR_DEVICE;
-    if (major != 10 || minor != 3) return KDA_ERR_DEVICE;
-    di.ok = true;
-  }
+  DeviceFacts df;
+  if (!current_device(&dev, &df)) return KDA_ERR_DEVICE;
   Layout L;
-  if (!make_layout(T, a->conv_width, a->record != 0, a->conv_f32 != 0, di.max_smem, L))
+  if (!make_layout(T, a->conv_width, a->record != 0, a->conv_f32 != 0, df.max_smem, L))
     return KDA_ERR_CONV_WIDTH;
 
   Params prm;
@@ -1272,27 +1254,27 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
 
   // Few items: one item per cluster of four CTAs (latency); many items: the
   // persistent kernel (bandwidth).
-  const bool split = a->path == 2 || (a->path == 0 && 4 * prm.items <= 2 * di.sms);
+  const bool split = a->path == 2 || (a->path == 0 && 4 * prm.items <= 2 * df.sms);
   if (split) return launch_split(a, stream);
-  const int grid = prm.items < di.sms ? prm.items : di.sms;
+  const int grid = prm.items < df.sms ? prm.items : df.sms;
   const int pdl = a->use_pdl ? 1 : 0;
   const bool rec = a->record != 0;
   switch (T) {
-    case 1: return launch_t<1, false>(prm, L, di, grid, pdl, stream);
-    case 2: return rec ? launch_t<2, true>(prm, L, di, grid, pdl, stream)
-                       : launch_t<2, false>(prm, L, di, grid, pdl, stream);
-    case 3: return rec ? launch_t<3, true>(prm, L, di, grid, pdl, stream)
-                       : launch_t<3, false>(prm, L, di, grid, pdl, stream);
-    case 4: return rec ? launch_t<4, true>(prm, L, di, grid, pdl, stream)
-                       : launch_t<4, false>(prm, L, di, grid, pdl, stream);
-    case 5: return rec ? launch_t<5, true>(prm, L, di, grid, pdl, stream)
-                       : launch_t<5, false>(prm, L, di, grid, pdl, stream);
-    case 6: return rec ? launch_t<6, true>(prm, L, di, grid, pdl, stream)
-                       : launch_t<6, false>(prm, L, di, grid, pdl, stream);
-    case 7: return rec ? launch_t<7, true>(prm, L, di, grid, pdl, stream)
-                       : launch_t<7, false>(prm, L, di, grid, pdl, stream);
-    default: return rec ? launch_t<8, true>(prm, L, di, grid, pdl, stream)
-                        : launch_t<8, false>(prm, L, di, grid, pdl, stream);
+    case 1: return launch_t<1, false>(prm, L, dev, df, grid, pdl, stream);
+    case 2: return rec ? launch_t<2, true>(prm, L, dev, df, grid, pdl, stream)
+                       : launch_t<2, false>(prm, L, dev, df, grid, pdl, stream);
+    case 3: return rec ? launch_t<3, true>(prm, L, dev, df, grid, pdl, stream)
+                       : launch_t<3, false>(prm, L, dev, df, grid, pdl, stream);
+    case 4: return rec ? launch_t<4, true>(prm, L, dev, df, grid, pdl, stream)
+                       : launch_t<4, false>(prm, L, dev, df, grid, pdl, stream);
+    case 5: return rec ? launch_t<5, true>(prm, L, dev, df, grid, pdl, stream)
+                       : launch_t<5, false>(prm, L, dev, df, grid, pdl, stream);
+    case 6: return rec ? launch_t<6, true>(prm, L, dev, df, grid, pdl, stream)
+                       : launch_t<6, false>(prm, L, dev, df, grid, pdl, stream);
+    case 7: return rec ? launch_t<7, true>(prm, L, dev, df, grid, pdl, stream)
+                       : launch_t<7, false>(prm, L, dev, df, grid, pdl, stream);
+    default: return rec ? launch_t<8, true>(prm, L, dev, df, grid, pdl, stream)
+                        : launch_t<8, false>(prm, L, dev, df, grid, pdl, stream);
   }
 }
 
