@@ -352,7 +352,7 @@ def run_pattern(args):
     schedule, no arithmetic), with the step's two stages and with three: the
     bandwidth ceiling of that access pattern, beside the measured copy peak."""
     import torch
-    from linear_attention_recurrent_kda_gb300.api import kda_probe_page_copy
+    from linear_attention_recurrent_kda_gb300.probe import kda_probe_page_copy
     from linear_attention_recurrent_kda_gb300.workloads import WORKLOADS, make_inputs
 
     from linear_attention_recurrent_kda_gb300.accounting import step_bytes
@@ -615,7 +615,7 @@ def main():
     # region: the ceiling of this access pattern, beside the copy peak.
     pattern = None
     if not w.record:
-        from linear_attention_recurrent_kda_gb300.api import kda_probe_page_copy
+        from linear_attention_recurrent_kda_gb300.probe import kda_probe_page_copy
         pslots = d["slots"].view(-1).contiguous() if T == 1 else d["slots"]
         pacc = d["accepted"] if T > 1 else None
 

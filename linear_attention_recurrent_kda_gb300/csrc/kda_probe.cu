@@ -12,8 +12,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/kda.h"
+#include "../../include/kda_probe.h"
 #include "kda_device.cuh"
+#include "kda_host.h"
 
 namespace kda {
 namespace probe {
@@ -120,9 +121,10 @@ __global__ void __launch_bounds__(32) page_copy_kernel(const __grid_constant__ k
 }
 
 template <int S>
-static int launch(const kda_probe_args *a, int grid, cudaStream_t stream) {
-  if (cudaFuncSetAttribute(page_copy_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           S * kPage) != cudaSuccess)
+static int launch(const kda_probe_args *a, int dev, int grid, cudaStream_t stream) {
+  static std::atomic<bool> configured[kMaxDevices];
+  if (!set_smem_limit_once(configured, dev, reinterpret_cast<const void *>(page_copy_kernel<S>),
+                           S * kPage))
     return KDA_ERR_LAUNCH;
   page_copy_kernel<S><<<grid, 32, S * kPage, stream>>>(*a);
   return cudaGetLastError() == cudaSuccess ? KDA_SUCCESS : KDA_ERR_LAUNCH;
@@ -141,16 +143,12 @@ static int run(const kda_probe_args *a, cudaStream_t stream) {
       (a->err && (reinterpret_cast<uintptr_t>(a->err) & 3u)) ||
       (a->tokens > 1 && (reinterpret_cast<uintptr_t>(a->accepted) & 3u)))
     return KDA_ERR_ALIGNMENT;
-  int dev = 0, major = 0, minor = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return KDA_ERR_DEVICE;
-  if (major != 10 || minor != 3) return KDA_ERR_DEVICE;
+  int dev = 0;
+  DeviceFacts df;
+  if (!current_device(&dev, &df)) return KDA_ERR_DEVICE;
   const int64_t items = static_cast<int64_t>(a->batch) * a->heads;
-  const int grid = static_cast<int>(items < sms ? items : sms);
-  return a->stages == 2 ? launch<2>(a, grid, stream) : launch<3>(a, grid, stream);
+  const int grid = static_cast<int>(items < df.sms ? items : df.sms);
+  return a->stages == 2 ? launch<2>(a, dev, grid, stream) : launch<3>(a, dev, grid, stream);
 }
 
 }  // namespace probe

@@ -32,8 +32,7 @@ KDA_DEVERR_ACCEPTED = 2
 KDA_DEVERR_TIMEOUT = 4
 
 EXPORTED = ("kda_decode", "kda_verify", "kda_recover", "kda_oproj",
-            "kda_selftest_wait_timeout", "kda_probe_page_copy", "kda_strerror",
-            "kda_abi_version")
+            "kda_selftest_wait_timeout", "kda_strerror", "kda_abi_version")
 
 
 class KdaArgs(ctypes.Structure):
@@ -79,16 +78,6 @@ class KdaOprojArgs(ctypes.Structure):
     ]
 
 
-class KdaProbeArgs(ctypes.Structure):
-    """Mirror of ``struct kda_probe_args``."""
-    _fields_ = [
-        ("batch", ctypes.c_int32), ("heads", ctypes.c_int32),
-        ("num_slots", ctypes.c_int32), ("stages", ctypes.c_int32),
-        ("state", _P), ("slots", _P), ("err", _P),
-        ("tokens", ctypes.c_int32), ("slot_cols", ctypes.c_int32), ("accepted", _P),
-    ]
-
-
 class KdaError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"KDA error {code}: {msg}")
@@ -117,8 +106,6 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.kda_recover.restype = ctypes.c_int
     lib.kda_oproj.argtypes = [ctypes.POINTER(KdaOprojArgs), ctypes.c_void_p]
     lib.kda_oproj.restype = ctypes.c_int
-    lib.kda_probe_page_copy.argtypes = [ctypes.POINTER(KdaProbeArgs), ctypes.c_void_p]
-    lib.kda_probe_page_copy.restype = ctypes.c_int
     lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
     lib.kda_selftest_wait_timeout.restype = ctypes.c_int
     lib.kda_strerror.argtypes = [ctypes.c_int]

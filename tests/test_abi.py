@@ -1,5 +1,8 @@
-"""The C-ABI library builds, loads and exports every function include/kda.h
-declares; host-side argument validation answers without touching a GPU."""
+"""The C-ABI libraries build, load and export every function their headers
+declare (include/kda.h: the product library; include/kda_probe.h: the
+measurement probe's own library, so that the product exports only the
+step's calls); host-side argument validation answers without touching a
+GPU."""
 from __future__ import annotations
 
 import os
@@ -9,27 +12,40 @@ import pytest
 
 from linear_attention_recurrent_kda_gb300 import build as kbuild
 from linear_attention_recurrent_kda_gb300 import lib as kl
+from linear_attention_recurrent_kda_gb300 import probe as kp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def declared_functions():
-    names = []
-    for fn in os.listdir(os.path.join(ROOT, "include")):
-        if fn.endswith(".h"):
-            text = open(os.path.join(ROOT, "include", fn)).read()
-            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(kda_\w+)\s*\(",
-                                text, flags=re.M)
+def declared_functions(header):
+    text = open(os.path.join(ROOT, "include", header)).read()
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(kda_\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))
+
+
+def test_every_header_is_covered():
+    assert sorted(f for f in os.listdir(os.path.join(ROOT, "include"))
+                  if f.endswith(".h")) == ["kda.h", "kda_probe.h"]
 
 
 def test_library_builds_and_exports_every_declared_symbol():
     kbuild.build()
     lib = kl.load()
-    names = declared_functions()
-    assert set(kl.EXPORTED) <= set(names)
+    names = declared_functions("kda.h")
+    assert set(kl.EXPORTED) == set(names)
     for n in names:
-        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+        assert hasattr(lib, n), f"{n} declared in include/kda.h but not exported"
+    # the bench instrument is not part of the product library
+    assert not hasattr(lib, "kda_probe_page_copy")
+
+
+def test_probe_library_exports_its_header():
+    kbuild.build()
+    lib = kp.load()
+    names = declared_functions("kda_probe.h")
+    assert set(kp.EXPORTED) == set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/kda_probe.h but not exported"
 
 
 def test_version_and_strerror():
@@ -125,7 +141,7 @@ def test_selftest_host_validation_without_gpu():
 
 
 def _pargs(**kw):
-    a = kl.KdaProbeArgs()
+    a = kp.KdaProbeArgs()
     a.batch, a.heads, a.num_slots, a.stages = 4, 2, 8, 2
     a.tokens, a.slot_cols = 1, 1
     a.state, a.slots = 1 << 20, 1 << 21
@@ -153,5 +169,5 @@ def _pargs(**kw):
     (dict(tokens=4, slot_cols=4, accepted=(1 << 23) + 2), kl.KDA_ERR_ALIGNMENT),
 ])
 def test_probe_host_validation_without_gpu(kw, code):
-    assert kl.call("kda_probe_page_copy", _pargs(**kw), 0) == code
-    assert kl.load().kda_probe_page_copy(None, None) == kl.KDA_ERR_NULL_ARGS
+    assert kp.call(_pargs(**kw), 0) == code
+    assert kp.load().kda_probe_page_copy(None, None) == kl.KDA_ERR_NULL_ARGS

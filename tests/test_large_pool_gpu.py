@@ -14,8 +14,8 @@ import pytest
 import torch
 
 from linear_attention_recurrent_kda_gb300 import lib as kl
-from linear_attention_recurrent_kda_gb300.api import (kda_probe_page_copy, kda_recover,
-                                                     step_from_inputs)
+from linear_attention_recurrent_kda_gb300.api import kda_recover, step_from_inputs
+from linear_attention_recurrent_kda_gb300.probe import kda_probe_page_copy
 from linear_attention_recurrent_kda_gb300.workloads import Workload, make_inputs
 from tests.parity import to_device
 

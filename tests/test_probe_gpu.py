@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from linear_attention_recurrent_kda_gb300 import lib as kl
-from linear_attention_recurrent_kda_gb300.api import kda_probe_page_copy
+from linear_attention_recurrent_kda_gb300.probe import kda_probe_page_copy
 from linear_attention_recurrent_kda_gb300.workloads import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
