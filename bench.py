@@ -162,15 +162,17 @@ def run_reference(args, workload):
     from linear_attention_recurrent_kda_gb300.workloads import make_inputs
     from tests.hostdata import to_oracle
     inp = to_oracle(make_inputs(workload))
-    threads = oracle.max_threads()
+    threads = args.oracle_threads or oracle.max_threads()
     rng = np.random.default_rng(0)
     order = rng.permutation(workload.items).astype(np.int32)
+    m = min(64, workload.items)
     t = time.perf_counter()
-    oracle.run(inp, mode="f32", items=np.sort(order[:64]), in_place=True,
+    oracle.run(inp, mode="f32", items=np.sort(order[:m]), in_place=True,
                threads=threads)
-    per_item = (time.perf_counter() - t) / 64
+    per_item = (time.perf_counter() - t) / m
     # size each step so the whole run stays near one minute of CPU time
     n = int(max(16, min(1024, 60.0 / (max(args.steps, 1) * per_item))))
+    n = min(n, workload.items)
     items = np.sort(order[:n])
     times = []
     for _ in range(args.steps):
@@ -197,13 +199,13 @@ def run_reference(args, workload):
     }
 
 
-def cpu_baseline(workload, budget_s=12.0):
+def cpu_baseline(workload, budget_s=12.0, threads=0):
     import numpy as np
     import oracle
     from linear_attention_recurrent_kda_gb300.workloads import make_inputs
     from tests.hostdata import to_oracle
     inp = to_oracle(make_inputs(workload))
-    threads = oracle.max_threads()
+    threads = threads or oracle.max_threads()
     rng = np.random.default_rng(1)
     n = min(workload.items, 1024)
     items = np.sort(rng.choice(workload.items, size=n, replace=False)).astype(np.int32)
@@ -441,6 +443,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="decode_b256_h32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-threads", type=int, default=0,
+                    help="OpenMP threads of the CPU oracle (reference arm and "
+                         "cpu_baseline); 0 = every host core")
     ap.add_argument("--op", default="step",
                     choices=["step", "recover", "oproj", "pattern"],
                     help="step: the decode/verify step (default); recover: the "
@@ -672,7 +677,7 @@ def main():
         "gpu_launches": args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(workload)
+        line["cpu_baseline"] = cpu_baseline(workload, threads=args.oracle_threads)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
