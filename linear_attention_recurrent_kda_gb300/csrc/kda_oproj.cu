@@ -37,7 +37,8 @@ namespace oproj {
 constexpr int kGroups = 4;      // rank groups of the partial sum
 constexpr int kMaxBlocks = 8;
 constexpr int kMaxTp = 64;
-constexpr int kMaxHidden = 7168;  // the page's hidden size: 896 threads a CTA
+constexpr int kMaxHidden = 7168;  // the page's hidden size
+constexpr int kThreads = 448;     // a CTA: two 8-feature chunks a thread at hidden 7168
 
 struct Params {
   int tp, tokens, vec, nb, has_delta;  // vec = hidden / 8
@@ -92,18 +93,12 @@ __device__ __forceinline__ void block_sum(float (&v)[N], float *red, float *tot)
   for (int i = 0; i < N; ++i) v[i] = tot[i];
 }
 
-template <int NB>
-__global__ void __launch_bounds__(kMaxHidden / 8) oproj_kernel(const __grid_constant__ Params p) {
-  constexpr int NR = NB > 0 ? 2 * NB + 2 : 1;
-  __shared__ float red[32 * NR];
-  __shared__ float tot[NR];
-  const int t = blockIdx.x;
-  const int i = threadIdx.x;
-  const int64_t row = static_cast<int64_t>(t) * p.vec + i;
-  const int64_t rank_stride = static_cast<int64_t>(p.tokens) * p.vec;
-
-  // --- 1. the new prefix (poll_sum / post): rank groups in order, each
-  // summed in rank order from its first rank.
+// Rank-group sum of the tp partials of one 8-feature chunk (poll_sum / post:
+// the groups in order, each summed in rank order from its first rank; up to
+// four 16-byte loads in flight), the new prefix p = BF16(sum) or BF16(prefix
+// + BF16(sum)), written back.
+__device__ __forceinline__ void prefix_chunk(const Params &p, int64_t row, int64_t rank_stride,
+                                             float (&pv)[8]) {
   const int per = (p.tp + kGroups - 1) / kGroups;
   const int S = per > 4 ? per : 4;
   float attn[8];
@@ -141,65 +136,102 @@ __global__ void __launch_bounds__(kMaxHidden / 8) oproj_kernel(const __grid_cons
       for (int k = 0; k < 8; ++k) attn[k] = __fadd_rn(attn[k], gs[k]);
     }
   }
-  float pv[8];
-  {
-    float old[8];
-    if (p.has_delta) unpack8(p.prefix[row], old);
+  float old[8];
+  if (p.has_delta) unpack8(p.prefix[row], old);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      float v = bf16_round(attn[k]);
-      if (p.has_delta) v = bf16_round(__fadd_rn(old[k], v));
-      pv[k] = v;
-    }
+  for (int k = 0; k < 8; ++k) {
+    float v = bf16_round(attn[k]);
+    if (p.has_delta) v = bf16_round(__fadd_rn(old[k], v));
+    pv[k] = v;
   }
   p.prefix[row] = pack8(pv);
-  float on[8];
-  unpack8(__ldg(p.out_norm + i), on);
+}
 
-  float y[8];
+// One CTA of kThreads threads per token row; thread i owns the 8-feature
+// chunks i and i + kThreads (one 16-byte vector of each BF16 row), so that two
+// CTAs fit on an SM (registers) and every row of a 256-row batch starts at
+// once; the new prefix and the mix wait in shared memory between the
+// CTA-wide sums.
+template <int NB>
+__global__ void __launch_bounds__(kThreads, 2) oproj_kernel(const __grid_constant__ Params p) {
+  constexpr int NR = NB > 0 ? 2 * NB + 2 : 1;
+  __shared__ float red[32 * NR];
+  __shared__ float tot[NR];
+  extern __shared__ __align__(16) float chunk_smem[];  // pv | mix: [2][vec][8]
+  const int t = blockIdx.x;
+  const int i = threadIdx.x;
+  const int nthr = blockDim.x;
+  const int64_t rank_stride = static_cast<int64_t>(p.tokens) * p.vec;
+  float *pvs = chunk_smem;                    // [vec][8] new prefix
+  float *mxs = chunk_smem + 8 * p.vec;        // [vec][8] unnormalised mix
+
+  // --- 1. the new prefix of every chunk this thread owns.
+#pragma unroll
+  for (int ch = 0; ch < 2; ++ch) {
+    const int c = i + ch * nthr;
+    if (c >= p.vec) break;
+    float pv[8];
+    prefix_chunk(p, static_cast<int64_t>(t) * p.vec + c, rank_stride, pv);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) pvs[c * 8 + k] = pv[k];
+  }
+
   if constexpr (NB == 0) {
     // RMSNorm of the prefix.
     float s[1] = {0.0f};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) s[0] = __fmaf_rn(pv[k], pv[k], s[0]);
+    for (int ch = 0; ch < 2; ++ch) {
+      const int c = i + ch * nthr;
+      if (c >= p.vec) break;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s[0] = __fmaf_rn(pvs[c * 8 + k], pvs[c * 8 + k], s[0]);
+    }
     block_sum<1>(s, red, tot);
     const float cp = rstd(s[0], p.out_eps, p.inv_hidden);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) y[k] = __fmul_rn(__fmul_rn(cp, pv[k]), on[k]);
-  } else {
-    // --- 2. combined weight, block and prefix logits (pre / post)
-    float w[8];
-    {
-      float nq[8], qq[8];
-      unpack8(__ldg(p.norm + i), nq);
-      unpack8(__ldg(p.query + i), qq);
+    for (int ch = 0; ch < 2; ++ch) {
+      const int c = i + ch * nthr;
+      if (c >= p.vec) break;
+      float on[8], y[8];
+      unpack8(__ldg(p.out_norm + c), on);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) w[k] = __fmul_rn(nq[k], qq[k]);
+      for (int k = 0; k < 8; ++k) y[k] = __fmul_rn(__fmul_rn(cp, pvs[c * 8 + k]), on[k]);
+      p.output[static_cast<int64_t>(t) * p.vec + c] = pack8(y);
     }
-    const uint4 *vb = p.blocks + static_cast<int64_t>(t) * NB * p.vec + i;
+  } else {
+    // --- 2. combined weight, block and prefix logits (pre / post).
     float acc[NR];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      float v[8];
-      unpack8(__ldg(vb + b * p.vec), v);
-      float ss = 0.0f, qk = 0.0f;
+    for (int r = 0; r < NR; ++r) acc[r] = 0.0f;
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      const int c = i + ch * nthr;
+      if (c >= p.vec) break;
+      float w[8];
+      {
+        float nq[8], qq[8];
+        unpack8(__ldg(p.norm + c), nq);
+        unpack8(__ldg(p.query + c), qq);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = __fmul_rn(nq[k], qq[k]);
+      }
+      const uint4 *vb = p.blocks + static_cast<int64_t>(t) * NB * p.vec + c;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        float v[8];
+        unpack8(__ldg(vb + b * p.vec), v);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          acc[2 * b] = __fmaf_rn(v[k], v[k], acc[2 * b]);
+          acc[2 * b + 1] = __fmaf_rn(v[k], w[k], acc[2 * b + 1]);
+        }
+      }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        ss = __fmaf_rn(v[k], v[k], ss);
-        qk = __fmaf_rn(v[k], w[k], qk);
+        const float pk = pvs[c * 8 + k];
+        acc[2 * NB] = __fmaf_rn(pk, pk, acc[2 * NB]);
+        acc[2 * NB + 1] = __fmaf_rn(pk, w[k], acc[2 * NB + 1]);
       }
-      acc[2 * b] = ss;
-      acc[2 * b + 1] = qk;
-    }
-    {
-      float pp = 0.0f, pw = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        pp = __fmaf_rn(pv[k], pv[k], pp);
-        pw = __fmaf_rn(pv[k], w[k], pw);
-      }
-      acc[2 * NB] = pp;
-      acc[2 * NB + 1] = pw;
     }
     block_sum<NR>(acc, red, tot);
     float logit[NB];
@@ -216,25 +248,33 @@ __global__ void __launch_bounds__(kMaxHidden / 8) oproj_kernel(const __grid_cons
       e[b] = exp_approx(__fsub_rn(logit[b], mx));
       esum = __fadd_rn(esum, e[b]);
     }
-    // The unnormalised block mix (blocks again, now from L1).
-    float mix[8];
+    // The unnormalised block mix (blocks again, now from L1/L2), mix . p and
+    // mix . mix.
+    float m2[2] = {0.0f, 0.0f};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) mix[k] = 0.0f;
+    for (int ch = 0; ch < 2; ++ch) {
+      const int c = i + ch * nthr;
+      if (c >= p.vec) break;
+      const uint4 *vb = p.blocks + static_cast<int64_t>(t) * NB * p.vec + c;
+      float mix[8];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      float v[8];
-      unpack8(__ldg(vb + b * p.vec), v);
+      for (int k = 0; k < 8; ++k) mix[k] = 0.0f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mix[k] = __fmaf_rn(e[b], v[k], mix[k]);
-    }
-    float m2[2] = {0.0f, 0.0f};  // mix . p, mix . mix
+      for (int b = 0; b < NB; ++b) {
+        float v[8];
+        unpack8(__ldg(vb + b * p.vec), v);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      m2[0] = __fmaf_rn(mix[k], pv[k], m2[0]);
-      m2[1] = __fmaf_rn(mix[k], mix[k], m2[1]);
+        for (int k = 0; k < 8; ++k) mix[k] = __fmaf_rn(e[b], v[k], mix[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        m2[0] = __fmaf_rn(mix[k], pvs[c * 8 + k], m2[0]);
+        m2[1] = __fmaf_rn(mix[k], mix[k], m2[1]);
+        mxs[c * 8 + k] = mix[k];
+      }
     }
     block_sum<2>(m2, red, tot);
-    // --- 3. the prefix merged into the softmax, the output coefficients
+    // --- 3. the prefix merged into the softmax, the output coefficients.
     const float top = fmaxf(mx, lp);
     const float alpha = exp_approx(__fsub_rn(mx, top));
     const float ep = exp_approx(__fsub_rn(lp, top));
@@ -247,15 +287,28 @@ __global__ void __launch_bounds__(kMaxHidden / 8) oproj_kernel(const __grid_cons
         rstd(quad, __fmul_rn(__fmul_rn(p.out_eps, den), den), p.inv_hidden);
     const float ca = __fmul_rn(alpha, scale), cp = __fmul_rn(ep, scale);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      y[k] = __fmul_rn(__fmaf_rn(ca, mix[k], __fmul_rn(cp, pv[k])), on[k]);
+    for (int ch = 0; ch < 2; ++ch) {
+      const int c = i + ch * nthr;
+      if (c >= p.vec) break;
+      float on[8], y[8];
+      unpack8(__ldg(p.out_norm + c), on);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        y[k] = __fmul_rn(__fmaf_rn(ca, mxs[c * 8 + k], __fmul_rn(cp, pvs[c * 8 + k])), on[k]);
+      p.output[static_cast<int64_t>(t) * p.vec + c] = pack8(y);
+    }
   }
-  p.output[row] = pack8(y);
 }
 
 template <int NB>
-static int launch(const Params &prm, int threads, cudaStream_t stream) {
-  oproj_kernel<NB><<<prm.tokens, threads, 0, stream>>>(prm);
+static int launch(const Params &prm, int dev, int threads, cudaStream_t stream) {
+  // the new prefix and the mix of every chunk: 2 x hidden floats
+  const int smem = prm.vec * 8 * 2 * static_cast<int>(sizeof(float));
+  static std::atomic<bool> configured[kMaxDevices];
+  if (!set_smem_limit_once(configured, dev, reinterpret_cast<const void *>(oproj_kernel<NB>),
+                           kMaxHidden * 2 * static_cast<int>(sizeof(float))))
+    return KDA_ERR_LAUNCH;
+  oproj_kernel<NB><<<prm.tokens, threads, smem, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? KDA_SUCCESS : KDA_ERR_LAUNCH;
 }
 
@@ -295,17 +348,18 @@ static int run(const kda_oproj_args *a, cudaStream_t stream) {
   prm.eps = a->eps;
   prm.out_eps = a->out_eps;
   prm.inv_hidden = 1.0f / static_cast<float>(a->hidden);
-  const int threads = prm.vec;  // a multiple of 32 (hidden % 256 == 0)
+  // two chunks a thread: ceil(vec / 2) threads rounded up to whole warps
+  const int threads = ((prm.vec + 1) / 2 + 31) / 32 * 32;
   switch (a->nb) {
-    case 0: return launch<0>(prm, threads, stream);
-    case 1: return launch<1>(prm, threads, stream);
-    case 2: return launch<2>(prm, threads, stream);
-    case 3: return launch<3>(prm, threads, stream);
-    case 4: return launch<4>(prm, threads, stream);
-    case 5: return launch<5>(prm, threads, stream);
-    case 6: return launch<6>(prm, threads, stream);
-    case 7: return launch<7>(prm, threads, stream);
-    default: return launch<8>(prm, threads, stream);
+    case 0: return launch<0>(prm, dev, threads, stream);
+    case 1: return launch<1>(prm, dev, threads, stream);
+    case 2: return launch<2>(prm, dev, threads, stream);
+    case 3: return launch<3>(prm, dev, threads, stream);
+    case 4: return launch<4>(prm, dev, threads, stream);
+    case 5: return launch<5>(prm, dev, threads, stream);
+    case 6: return launch<6>(prm, dev, threads, stream);
+    case 7: return launch<7>(prm, dev, threads, stream);
+    default: return launch<8>(prm, dev, threads, stream);
   }
 }
 
