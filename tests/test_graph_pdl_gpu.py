@@ -51,8 +51,12 @@ class Launch:
                               device="cuda")
         self.dbg = torch.zeros((B, H, T, 4, 128), dtype=torch.bfloat16, device="cuda")
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        self.step = step_from_inputs(d, self.out, err=self.err, dbg=self.dbg,
-                                     use_pdl=use_pdl)
+        self.rec_u = self.rec_kg = None
+        if d["record"]:
+            self.rec_u = torch.zeros((B, H, T, 128), dtype=torch.float32, device="cuda")
+            self.rec_kg = torch.zeros((B, H, T, 256), dtype=torch.bfloat16, device="cuda")
+        self.step = step_from_inputs(d, self.out, rec_u=self.rec_u, rec_kg=self.rec_kg,
+                                     err=self.err, dbg=self.dbg, use_pdl=use_pdl)
 
     def pools(self):
         """Host copies of the current pools (inputs of a following step)."""
@@ -61,19 +65,30 @@ class Launch:
 
     def result(self):
         torch.cuda.synchronize()
-        return {"output": bits(self.out), "state": self.d["state"].cpu().numpy(),
-                "conv_state": bits(self.d["conv_state"]), "err": int(self.err.item()),
-                "dbg": bits(self.dbg)}
+        res = {"output": bits(self.out), "state": self.d["state"].cpu().numpy(),
+               "conv_state": bits(self.d["conv_state"]), "err": int(self.err.item()),
+               "dbg": bits(self.dbg)}
+        if self.rec_u is not None:
+            res["rec_u"] = self.rec_u.cpu().numpy()
+            res["rec_kg"] = bits(self.rec_kg)
+        return res
 
     def snapshot(self):
         torch.cuda.synchronize()
         return [self.d["state"].clone(), self.d["conv_state"].clone(), self.out.clone()]
 
 
-@pytest.mark.parametrize("tokens", [1, 3])
-def test_cuda_graph_replay_matches_the_oracle(tokens):
-    w = wl(tokens=tokens, slot_layout="decode" if tokens == 1 else "verify",
-           conv_width=tokens + 2, num_slots=48 * tokens + 9)
+def layout(tokens, record=False):
+    if record:
+        return dict(tokens=tokens, slot_layout="checkpoint", conv_width=tokens + 2,
+                    record=True, gate_mode=1, has_bias=True, num_slots=60)
+    return dict(tokens=tokens, slot_layout="decode" if tokens == 1 else "verify",
+                conv_width=tokens + 2, num_slots=48 * tokens + 9)
+
+
+@pytest.mark.parametrize("tokens,record", [(1, False), (3, False), (4, True)])
+def test_cuda_graph_replay_matches_the_oracle(tokens, record):
+    w = wl(**layout(tokens, record))
     inp = make_inputs(w)
     eager, graphed = Launch(inp), Launch(inp)
     # one eager call on a throwaway copy configures the kernel before capture
@@ -95,10 +110,9 @@ def test_cuda_graph_replay_matches_the_oracle(tokens):
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("tokens", [1, 4])
-def test_pdl_after_a_kernel_that_rewrites_the_inputs(tokens):
-    w = wl(tokens=tokens, slot_layout="decode" if tokens == 1 else "verify",
-           conv_width=tokens + 2, num_slots=48 * tokens + 9)
+@pytest.mark.parametrize("tokens,record", [(1, False), (4, False), (4, True)])
+def test_pdl_after_a_kernel_that_rewrites_the_inputs(tokens, record):
+    w = wl(**layout(tokens, record))
     inp = make_inputs(w)
     g = torch.Generator().manual_seed(9)
     new = dict(inp)
