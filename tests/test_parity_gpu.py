@@ -247,12 +247,12 @@ def test_full_size_workloads_sampled(name, path):
     path is the one the benchmark times): its pools, outputs, records and
     error word equal, bit for bit, those of a launch with the dbg buffer on
     the same inputs, which the anchored comparison checks against the oracle
-    on a seeded sample of items one by one (plus every padded item); the
+    on a seeded sample of 1024 items one by one (plus every padded item); the
     product launch itself is also compared with the oracle unanchored."""
     w = WORKLOADS[name]
     inp = make_inputs(w)
     rng = np.random.default_rng(5)
-    items = np.sort(rng.choice(w.items, size=96, replace=False))
+    items = np.sort(rng.choice(w.items, size=1024, replace=False))
     prod = run_gpu(inp, dbg=False, path=path)
     rep = unanchored(inp, prod, items=items)
     checked = run_gpu(inp, dbg=True, path=path)
