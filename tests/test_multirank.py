@@ -82,3 +82,18 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_counts_only_the_items_it_runs():
+    """The reference arm's sample is capped at the workload's items, so a
+    small workload's rate counts the items the oracle actually stepped."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    from linear_attention_recurrent_kda_gb300.workloads import WORKLOADS
+    args = argparse.Namespace(steps=1, warmup=0, gpus=1, oracle_threads=1)
+    line = bench.run_reference(args, WORKLOADS["decode_b4_h8"])
+    assert line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["sample"].startswith("32 of 32 items")
+    # value = items stepped / time of a step, and ms_per_step the whole workload
+    assert abs(line["value"] * line["ms_per_step"] * 1e-3 - 32) < 1e-6 * 32
