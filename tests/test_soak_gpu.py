@@ -1,10 +1,13 @@
 """Repeated launches from restored pools reproduce the first launch's bits.
 
-Each workload runs 300 times; before every launch the state and conv pools
+Each workload runs 300 times (KDA_SOAK_LAUNCHES overrides the count for a
+longer run); before every launch the state and conv pools
 are restored and the outputs and records are filled with NaN, so any
 launch-to-launch difference (a race between the kernel's roles, a stale
 stage, a missed barrier) shows up as changed bits."""
 from __future__ import annotations
+
+import os
 
 import pytest
 import torch
@@ -14,7 +17,7 @@ from linear_attention_recurrent_kda_gb300.workloads import WORKLOADS, make_input
 
 pytestmark = pytest.mark.gpu
 
-N = 300
+N = int(os.environ.get("KDA_SOAK_LAUNCHES", "300"))
 
 
 def _bits(t):
