@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 5
+#define KDA_ABI_VERSION 6
 #define KDA_DK 128
 #define KDA_MAX_TOKENS 8
 
@@ -147,6 +147,17 @@ typedef struct kda_args {
                             /* are read as stored and the new window is      */
                             /* written as FP32 (the page's conv_type is the  */
                             /* pool's element type)                          */
+  int32_t *sched;           /* optional i32 [2] device scheduler words, zero */
+                            /* before first use; the kernel leaves them zero */
+                            /* when it ends.  With them the persistent path  */
+                            /* hands the last eighth of the items out one at */
+                            /* a time to whichever CTA is free (same bits as */
+                            /* without); NULL = fixed contiguous ranges.     */
+                            /* Launches that may run at the same time (other */
+                            /* streams, other threads) need separate words;  */
+                            /* launches in order on one stream, PDL-chained  */
+                            /* or captured in a graph, may share them.       */
+                            /* Ignored by the cluster-split path (path 2).   */
 } kda_args;
 
 /* One decode step (tokens == 1) on `stream` (a cudaStream_t; NULL = the

@@ -21,8 +21,9 @@ extern "C" {
  * writes: tokens == 1 (decode) reads state[slots[r], h] and writes it back
  * in place; tokens T > 1 (verify) reads state[slots[r, accepted[r]-1], h]
  * and writes it to state[slots[r, t], h] for each t < T whose slot is > 0.
- * One CTA per SM over contiguous item ranges with a ring of `stages` (2 or
- * 3) pages, as the step schedules its pages.  Decode leaves the pool's
+ * One CTA per SM over contiguous item ranges (and, with `sched`, the
+ * step's shared items) with a ring of `stages` (2 or 3) pages, as the step
+ * schedules its pages.  Decode leaves the pool's
  * values unchanged.  Its bandwidth bounds what the step's page traffic can
  * reach.
  *   state     float [num_slots, heads, 128, 128], 16-byte aligned, in/out
@@ -43,6 +44,9 @@ typedef struct kda_probe_args {
   int32_t *err;
   int32_t tokens, slot_cols;  /* 1 and 1 for decode                         */
   const int32_t *accepted;    /* tokens > 1 only                             */
+  int32_t *sched;             /* optional i32 [2] scheduler words, as in     */
+                              /* kda_args: the step's split between ranges   */
+                              /* and shared items; NULL = ranges only        */
 } kda_probe_args;
 int kda_probe_page_copy(const kda_probe_args *args, void *stream);
 

@@ -56,6 +56,12 @@ class KdaStep:
     Validates once, keeps the filled ``kda_args`` and launches with
     ``__call__(stream)``; reuse it across steps that read the same buffers
     (the tensors' contents may change between calls, their storage may not).
+
+    ``sched``: the persistent kernel's scheduler words (int32 [2], zero before
+    first use; ``kda_args.sched``).  By default the step allocates its own,
+    so its launches balance the last items over the CTAs; pass a tensor to
+    share one between steps launched in order on one stream, or
+    ``balance=False`` for fixed contiguous ranges only (same bits).
     """
 
     def __init__(self, *, x, conv_weight, conv_state, f_a, f_b, beta, a_log,
@@ -64,7 +70,7 @@ class KdaStep:
                  tokens: int = 1, accepted=None, conv_bias=None,
                  gate_mode: int = 0, record: bool = False, rec_u=None,
                  rec_kg=None, err=None, dbg=None, use_pdl: bool = False,
-                 path: int = 0):
+                 path: int = 0, sched=None, balance: bool = True):
         bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
         T = int(tokens)
         if not 1 <= T <= 8:
@@ -111,12 +117,15 @@ class KdaStep:
         _check("err", err, i32, allow_none=True)
         _check("dbg", dbg, bf, (B, H, T, 4, DK), allow_none=True)
         dev = output.device
+        if sched is None and balance:
+            sched = torch.zeros(2, dtype=i32, device=dev)
+        _check("sched", sched, i32, (2,), allow_none=True)
         _same_device(dev, x=x, conv_weight=conv_weight, conv_bias=conv_bias,
                      conv_state=conv_state, f_a=f_a, f_b=f_b, beta=beta, a_log=a_log,
                      dt_bias=dt_bias, slots=slots, state=state, gate=gate,
                      norm_weight=norm_weight, accepted=accepted if T > 1 else None,
                      rec_u=rec_u if record else None, rec_kg=rec_kg if record else None,
-                     err=err, dbg=dbg)
+                     err=err, dbg=dbg, sched=sched)
 
         a = _lib.KdaArgs()
         a.batch, a.heads, a.tokens = B, H, T
@@ -134,13 +143,14 @@ class KdaStep:
         a.err, a.dbg = _ptr(err), _ptr(dbg)
         a.path = int(path)
         a.conv_f32 = int(conv_state.dtype == f32)
+        a.sched = _ptr(sched)
         self.args = a
         self.entry = "kda_decode" if T == 1 else "kda_verify"
         self.device = dev
         # keep the tensors alive as long as the prepared step
         self._keep = (x, conv_weight, conv_state, f_a, f_b, beta, a_log, dt_bias,
                       slots, state, output, gate, norm_weight, accepted,
-                      conv_bias, rec_u, rec_kg, err, dbg)
+                      conv_bias, rec_u, rec_kg, err, dbg, sched)
 
     def __call__(self, stream: Optional[torch.cuda.Stream] = None) -> None:
         # the library launches on the current device: make it the tensors' one
@@ -172,7 +182,8 @@ INPUT_KEYS = ("x", "conv_weight", "conv_bias", "conv_state", "f_a", "f_b", "beta
 
 def step_from_inputs(dev_inputs: Dict[str, object], output: torch.Tensor, *,
                      rec_u=None, rec_kg=None, err=None, dbg=None,
-                     use_pdl: bool = False, path: int = 0) -> KdaStep:
+                     use_pdl: bool = False, path: int = 0, sched=None,
+                     balance: bool = True) -> KdaStep:
     """A ``KdaStep`` from a device copy of a seeded workload's input dict."""
     d = dev_inputs
     T = int(d["tokens"])
@@ -185,7 +196,8 @@ def step_from_inputs(dev_inputs: Dict[str, object], output: torch.Tensor, *,
         accepted=d.get("accepted") if T > 1 else None,
         conv_bias=d.get("conv_bias") if d.get("has_bias") else None,
         gate_mode=int(d["gate_mode"]), record=bool(d["record"]), rec_u=rec_u,
-        rec_kg=rec_kg, err=err, dbg=dbg, use_pdl=use_pdl, path=path)
+        rec_kg=rec_kg, err=err, dbg=dbg, use_pdl=use_pdl, path=path, sched=sched,
+        balance=balance)
 
 
 def kda_recover(*, state, src_slots, dst_slots, accepted, rec_u, rec_kg, a_log,

@@ -55,15 +55,24 @@ __device__ __forceinline__ bool probe_resolve(const kda_probe_args &a, int n, Pr
   return !bad;
 }
 
+// Items dyn0 .. items-1 go one at a time to the CTA that asks first when the
+// scheduler words are given (the step's schedule, same rule for dyn0).
 template <int S>
-__global__ void __launch_bounds__(32) page_copy_kernel(const __grid_constant__ kda_probe_args a) {
+__global__ void __launch_bounds__(32) page_copy_kernel(const __grid_constant__ kda_probe_args a,
+                                                       int dyn0) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full[S];
   __shared__ uint32_t abort_flag;
   if (threadIdx.x != 0) return;
   const int items = a.batch * a.heads, G = gridDim.x;
-  const int n0 = static_cast<int>(static_cast<int64_t>(items) * blockIdx.x / G);
-  const int n1 = static_cast<int>(static_cast<int64_t>(items) * (blockIdx.x + 1) / G);
+  int n0, n1;
+  if (a.sched) {
+    n0 = (dyn0 / G) * static_cast<int>(blockIdx.x);
+    n1 = n0 + dyn0 / G;
+  } else {
+    n0 = static_cast<int>(static_cast<int64_t>(items) * blockIdx.x / G);
+    n1 = static_cast<int>(static_cast<int64_t>(items) * (blockIdx.x + 1) / G);
+  }
   abort_flag = 0u;
   for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -71,11 +80,21 @@ __global__ void __launch_bounds__(32) page_copy_kernel(const __grid_constant__ k
     const int h = n / a.batch;
     return a.state + (static_cast<int64_t>(slot) * a.heads + h) * (kPage / 4);
   };
-  // The next live item at or after n (n1 when none), resolved into `it`.
-  auto next_live = [&](int n, ProbeItem &it) -> int {
+  // The CTA's next live item after its cursor n (its range, then shared
+  // items), resolved into `it`; -1 when none is left.
+  bool drained = a.sched == nullptr;
+  auto next_live = [&](int &n, ProbeItem &it) -> int {
     for (; n < n1; ++n)
-      if (probe_resolve(a, n, it)) break;
-    return n;
+      if (probe_resolve(a, n, it)) return n++;
+    while (!drained) {
+      const int m = dyn0 + atomicAdd(a.sched, 1);
+      if (m >= items) {
+        drained = true;
+        break;
+      }
+      if (probe_resolve(a, m, it)) return m;
+    }
+    return -1;
   };
   const uint64_t pol = policy_evict_first();
   // The j-th live item of the range goes through stage j % S.
@@ -83,9 +102,9 @@ __global__ void __launch_bounds__(32) page_copy_kernel(const __grid_constant__ k
   ProbeItem res[S];
   int loaded = 0, n = n0;
   for (int s = 0; s < S; ++s) {
-    n = next_live(n, res[s]);
-    if (n >= n1) break;
-    item[s] = n++;
+    const int m = next_live(n, res[s]);
+    if (m < 0) break;
+    item[s] = m;
     mbar_arrive_expect_tx(&full[s], kPage);
     bulk_g2s(smem + s * kPage, page(item[s], res[s].src), kPage, &full[s]);
     ++loaded;
@@ -108,9 +127,9 @@ __global__ void __launch_bounds__(32) page_copy_kernel(const __grid_constant__ k
       // Refill the stage of item i-1 once its stores have read it.
       bulk_wait_read(1);
       const int ps = (i - 1) % S;
-      n = next_live(n, res[ps]);
-      if (n < n1) {
-        item[ps] = n++;
+      const int m = next_live(n, res[ps]);
+      if (m >= 0) {
+        item[ps] = m;
         mbar_arrive_expect_tx(&full[ps], kPage);
         bulk_g2s(smem + ps * kPage, page(item[ps], res[ps].src), kPage, &full[ps]);
         ++loaded;
@@ -118,15 +137,23 @@ __global__ void __launch_bounds__(32) page_copy_kernel(const __grid_constant__ k
     }
   }
   bulk_wait_all();
+  if (a.sched) {
+    // The last CTA zeroes the scheduler words for the next launch.
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1) == G - 1) {
+      atomicExch(a.sched, 0);
+      atomicExch(a.sched + 1, 0);
+    }
+  }
 }
 
 template <int S>
-static int launch(const kda_probe_args *a, int dev, int grid, cudaStream_t stream) {
+static int launch(const kda_probe_args *a, int dev, int grid, int dyn0, cudaStream_t stream) {
   static std::atomic<bool> configured[kMaxDevices];
   if (!set_smem_limit_once(configured, dev, reinterpret_cast<const void *>(page_copy_kernel<S>),
                            S * kPage))
     return KDA_ERR_LAUNCH;
-  page_copy_kernel<S><<<grid, 32, S * kPage, stream>>>(*a);
+  page_copy_kernel<S><<<grid, 32, S * kPage, stream>>>(*a, dyn0);
   return cudaGetLastError() == cudaSuccess ? KDA_SUCCESS : KDA_ERR_LAUNCH;
 }
 
@@ -141,14 +168,20 @@ static int run(const kda_probe_args *a, cudaStream_t stream) {
   if (!a->state || !a->slots || (a->tokens > 1 && !a->accepted)) return KDA_ERR_NULL_POINTER;
   if ((reinterpret_cast<uintptr_t>(a->state) & 15u) || (reinterpret_cast<uintptr_t>(a->slots) & 3u) ||
       (a->err && (reinterpret_cast<uintptr_t>(a->err) & 3u)) ||
-      (a->tokens > 1 && (reinterpret_cast<uintptr_t>(a->accepted) & 3u)))
+      (a->tokens > 1 && (reinterpret_cast<uintptr_t>(a->accepted) & 3u)) ||
+      (reinterpret_cast<uintptr_t>(a->sched) & 3u))
     return KDA_ERR_ALIGNMENT;
   int dev = 0;
   DeviceFacts df;
   if (!current_device(&dev, &df)) return KDA_ERR_DEVICE;
   const int64_t items = static_cast<int64_t>(a->batch) * a->heads;
   const int grid = static_cast<int>(items < df.sms ? items : df.sms);
-  return a->stages == 2 ? launch<2>(a, dev, grid, stream) : launch<3>(a, dev, grid, stream);
+  // The step's split between contiguous ranges and shared items.
+  const bool wide = a->tokens == 1 && items >= 32 * static_cast<int64_t>(grid);
+  const int dyn0 = a->sched ? static_cast<int>(items * (wide ? 7 : 8) / 8 / grid) * grid
+                            : static_cast<int>(items);
+  return a->stages == 2 ? launch<2>(a, dev, grid, dyn0, stream)
+                        : launch<3>(a, dev, grid, dyn0, stream);
 }
 
 }  // namespace probe

@@ -72,13 +72,14 @@ constexpr int kMaxStages = 3;
 constexpr int kSlots = 2;                         // front -> recurrence hand-off
 constexpr int kMaxQuarterBufs = 4;                // 16 KiB quarter-page store ring
 constexpr uint32_t kQuarterBytes = kPageBytes / 4;
-constexpr int kLive = 0, kPad = 1, kError = 2;
+constexpr int kLive = 0, kPad = 1, kError = 2, kEnd = 3;  // kEnd: no more items
 
 static_assert(kRecThreads * kRecRegs + kFrontThreads * kFrontRegs + 128 * kProducerRegs <=
                   kThreads * 128,
               "register split exceeds the launch allocation");
 
 struct __align__(16) ItemDesc {
+  int32_t item;  // n = h * batch + r
   int32_t status;
   int32_t slot;
   int32_t conv_slot;
@@ -91,6 +92,13 @@ struct Params {
   int32_t batch, heads, num_slots, conv_width, slot_cols, gate_mode, has_bias;
   int32_t conv_f32;  // conv pool element: FP32 (1) or BF16 (0)
   int32_t items, stages;
+  // Item schedule: CTA b owns items [b*q, b*q + q) (q = dyn0 / grid); with a
+  // scheduler word pair, items dyn0 .. items-1 then go one at a time to the
+  // CTA whose producer asks first (sched[0] counts them out, sched[1] counts
+  // finished CTAs; the last CTA zeroes both).  Without one, the items are
+  // split into contiguous ranges only.
+  int32_t *sched;
+  int32_t dyn0;
   uint32_t stage_bytes, conv_off, x_off, gate_off, fa_off;
   uint32_t bar_off, desc_off, slot_off, slot_bytes, scratch_off, rscratch_off;
   uint32_t qbuf_off;
@@ -246,11 +254,21 @@ template <int T, bool RECORD>
 __device__ void producer_role(const Params &p, uint8_t *smem, Ctrl *ctl,
                               ItemDesc *desc, int n0, int n1) {
   const int S = p.stages;
-  const int count = n1 - n0;
   const uint64_t pol = policy_evict_first();
-  const int pro = count < S ? count : S;
+  const int pro = (n1 - n0) < S ? (n1 - n0) : S;
   int issued = 0;
   bool aborted = false;
+  bool drained = p.sched == nullptr;  // no shared items left to ask for
+  // The CTA's k-th item: its own range first, then shared items (after the
+  // wait on the preceding kernel); -1 once none is left.
+  auto item_at = [&](int k) -> int {
+    if (n0 + k < n1) return n0 + k;
+    if (drained) return -1;
+    const int n = p.dyn0 + atomicAdd(p.sched, 1);
+    if (n < p.items) return n;
+    drained = true;
+    return -1;
+  };
 
   // Prologue: the first pages go out before waiting on the preceding kernel
   // (the state pool, slots and accepted must not be its outputs); nothing is
@@ -258,6 +276,7 @@ __device__ void producer_role(const Params &p, uint8_t *smem, Ctrl *ctl,
   int pro_flags = 0;
   for (int k = 0; k < pro; ++k) {
     ItemDesc &d = desc[k];
+    d.item = n0 + k;
     pro_flags |= resolve_item<T, RECORD>(p, n0 + k, d);
     if (d.status == kLive) {
       mbar_expect_tx(&ctl->full[k], kPageBytes);
@@ -279,40 +298,59 @@ __device__ void producer_role(const Params &p, uint8_t *smem, Ctrl *ctl,
     }
     ++issued;
   }
-  for (int k = pro; k < count; ++k) {
+  for (int k = pro;; ++k) {
     const int stage = k % S;
     const uint32_t round = static_cast<uint32_t>(k / S);
+    const int n = item_at(k);
     // Verify items resolve their slots (dependent global loads) while the
     // stage is still busy; decode items after the wait (measured faster).
     ItemDesc nd;
     int flags = 0;
-    if (T > 1) {
-      flags = resolve_item<T, RECORD>(p, n0 + k, nd);
-      load_beta<T>(p, n0 + k, nd);
+    if (T > 1 && n >= 0) {
+      flags = resolve_item<T, RECORD>(p, n, nd);
+      load_beta<T>(p, n, nd);
     }
-    if (!mbar_wait(&ctl->empty[stage], (round - 1u) & 1u, &ctl->abort)) {
+    if (round > 0 && !mbar_wait(&ctl->empty[stage], (round - 1u) & 1u, &ctl->abort)) {
       aborted = true;
       break;
     }
     ItemDesc &d = desc[stage];
+    if (n < 0) {
+      // End of the stream for the front and the recurrence.
+      d.item = -1;
+      d.status = kEnd;
+      mbar_arrive(&ctl->full[stage]);
+      break;
+    }
     if (T > 1) {
       d = nd;
     } else {
-      flags = resolve_item<T, RECORD>(p, n0 + k, d);
-      load_beta<T>(p, n0 + k, d);
+      flags = resolve_item<T, RECORD>(p, n, d);
+      load_beta<T>(p, n, d);
     }
+    d.item = n;
     if (flags && p.err) atomicOr(p.err, flags);
     uint8_t *st = smem + static_cast<size_t>(stage) * p.stage_bytes;
     if (d.status == kLive) {
       mbar_arrive_expect_tx(&ctl->full[stage], kPageBytes + small_bytes<T>(p));
-      issue_page(p, st, n0 + k, d, &ctl->full[stage], pol);
-      issue_small<T>(p, st, n0 + k, d, &ctl->full[stage]);
+      issue_page(p, st, n, d, &ctl->full[stage], pol);
+      issue_small<T>(p, st, n, d, &ctl->full[stage]);
     } else {
       mbar_arrive(&ctl->full[stage]);
     }
     ++issued;
   }
   griddep_launch_dependents();
+  if (p.sched) {
+    // This CTA asks for no more shared items; the last CTA to get here zeroes
+    // the scheduler words for the next launch (every request of this launch
+    // precedes its CTA's count).
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(p.sched, 0);
+      atomicExch(p.sched + 1, 0);
+    }
+  }
   if (aborted || ctl->abort) {
     if (p.err) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
     // Drain: every copy issued into a stage must land before the CTA exits.
@@ -648,7 +686,7 @@ __device__ __forceinline__ void front_epilogue(const Params &p, const SlotView<T
 
 template <int T, bool RECORD>
 __device__ void front_role(const Params &p, uint8_t *smem, Ctrl *ctl,
-                           const ItemDesc *desc, int n0, int n1) {
+                           const ItemDesc *desc) {
   const int c = threadIdx.x - kRecThreads;  // channel 0..127
   const int S = p.stages;
   const int64_t dim = static_cast<int64_t>(p.heads) * kDk;
@@ -659,7 +697,7 @@ __device__ void front_role(const Params &p, uint8_t *smem, Ctrl *ctl,
   FrontConst fc;
   int cur_head = -1;
   int j = 0;  // live items seen
-  for (int k = 0; k < n1 - n0; ++k) {
+  for (int k = 0;; ++k) {
     const int stage = k % S;
     const uint32_t round = static_cast<uint32_t>(k / S);
     const bool ok = mbar_wait(&ctl->full[stage], round & 1u, &ctl->abort);
@@ -667,14 +705,15 @@ __device__ void front_role(const Params &p, uint8_t *smem, Ctrl *ctl,
       aborted = true;
       break;
     }
+    const ItemDesc &dsc = desc[stage];
+    if (dsc.status == kEnd) break;
     // A landed stage means the producer has passed its wait on the preceding
     // kernel (programmatic dependent launch): inputs other than the state
     // pool, slots and accepted may be read from here on.
     if (k == 0)
       nw = bf16_bits_to_float(__ldg(reinterpret_cast<const uint16_t *>(p.norm_weight) + c));
-    const int n = n0 + k;
+    const int n = dsc.item;
     const int h = n / p.batch;
-    const ItemDesc &dsc = desc[stage];
     if (dsc.status != kLive) {
       const int r = n - h * p.batch;
       mbar_arrive(&ctl->empty[stage]);
@@ -831,7 +870,7 @@ __device__ __forceinline__ void pass_update_dot_decay_dot(
 
 template <int T, bool RECORD>
 __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
-                                const ItemDesc *desc, int n0, int n1) {
+                                const ItemDesc *desc) {
   const int tid = threadIdx.x;  // 0..255
   const int lane = tid & 31;
   const int g8 = tid >> 3, l8 = tid & 7;
@@ -840,7 +879,7 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
   const uint64_t pol = policy_evict_first();
   int j = 0;
   uint32_t wq = 0;  // decode: quarters handed to the store thread so far
-  for (int k = 0; k < n1 - n0; ++k) {
+  for (int k = 0;; ++k) {
     const int stage = k % S;
     const uint32_t round = static_cast<uint32_t>(k / S);
     bool ok = mbar_wait(&ctl->full[stage], round & 1u, &ctl->abort);
@@ -848,16 +887,17 @@ __device__ void recurrence_role(const Params &p, uint8_t *smem, Ctrl *ctl,
     // a non-live item's stage right after it, and the producer then rewrites
     // the descriptor; a read after that could see the next item's status and
     // split the recurrence warps between two barrier sequences.
-    const bool live = ok && desc[stage].status == kLive;
+    const int status = ok ? desc[stage].status : kError;
+    const int n = ok ? desc[stage].item : 0;
     if (rec_sync_or(!ok)) {
       if (T > 1 && !RECORD && tid == 0) bulk_wait_all();
       return;
     }
-    if (!live) {
+    if (status == kEnd) break;
+    if (status != kLive) {
       if (tid == 0) mbar_arrive(&ctl->empty[stage]);
       continue;
     }
-    const int n = n0 + k;
     const int h = n / p.batch;
     const int r = n - h * p.batch;
     const int64_t item = static_cast<int64_t>(r) * p.heads + h;
@@ -1053,8 +1093,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_step_kernel(const __grid_cons
   Ctrl *ctl = reinterpret_cast<Ctrl *>(smem + p.bar_off);
   ItemDesc *desc = reinterpret_cast<ItemDesc *>(smem + p.desc_off);
   const int G = gridDim.x;
-  const int n0 = static_cast<int>((static_cast<int64_t>(p.items) * blockIdx.x) / G);
-  const int n1 = static_cast<int>((static_cast<int64_t>(p.items) * (blockIdx.x + 1)) / G);
+  int n0, n1;
+  if (p.sched) {
+    const int q = p.dyn0 / G;
+    n0 = q * static_cast<int>(blockIdx.x);
+    n1 = n0 + q;
+  } else {
+    n0 = static_cast<int>((static_cast<int64_t>(p.items) * blockIdx.x) / G);
+    n1 = static_cast<int>((static_cast<int64_t>(p.items) * (blockIdx.x + 1)) / G);
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&ctl->full[s], 1);
@@ -1074,10 +1121,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_step_kernel(const __grid_cons
   __syncthreads();
   if (threadIdx.x < kRecThreads) {
     regs_inc<kRecRegs>();
-    recurrence_role<T, RECORD>(p, smem, ctl, desc, n0, n1);
+    recurrence_role<T, RECORD>(p, smem, ctl, desc);
   } else if (threadIdx.x < kProducer) {
     regs_inc<kFrontRegs>();
-    front_role<T, RECORD>(p, smem, ctl, desc, n0, n1);
+    front_role<T, RECORD>(p, smem, ctl, desc);
   } else {
     regs_dec<kProducerRegs>();
     if (threadIdx.x == kProducer) producer_role<T, RECORD>(p, smem, ctl, desc, n0, n1);
@@ -1195,7 +1242,8 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
       (a->accepted && !aligned(a->accepted, 4)) ||
       (a->has_bias && !aligned(a->conv_bias, 2)) ||
       (a->rec_u && !aligned(a->rec_u, 4)) || (a->rec_kg && !aligned(a->rec_kg, 2)) ||
-      (a->err && !aligned(a->err, 4)) || (a->dbg && !aligned(a->dbg, 2)))
+      (a->err && !aligned(a->err, 4)) || (a->dbg && !aligned(a->dbg, 2)) ||
+      (a->sched && !aligned(a->sched, 4)))
     return KDA_ERR_ALIGNMENT;
 
   int dev = 0;
@@ -1215,6 +1263,7 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
   prm.has_bias = a->has_bias ? 1 : 0;
   prm.items = a->batch * a->heads;
   prm.stages = L.stages;
+  prm.sched = a->sched;
   prm.stage_bytes = L.stage_bytes;
   prm.conv_off = L.conv_off;
   prm.x_off = L.x_off;
@@ -1257,6 +1306,17 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
   const bool split = a->path == 2 || (a->path == 0 && 4 * prm.items <= 2 * df.sms);
   if (split) return launch_split(a, stream);
   const int grid = prm.items < df.sms ? prm.items : df.sms;
+  // With a scheduler word pair, each CTA keeps a contiguous range (per-head
+  // constants stay in registers, the first pages can go out before the wait
+  // on the preceding kernel) and the items past the ranges are handed out one
+  // at a time, so CTAs on slower SMs or with slower pages take fewer.  A
+  // shared item usually changes the CTA's head (its constants are reloaded),
+  // so the ranges cover 7/8 of the items where the CTAs' finishing times
+  // spread most (decode with 32 or more items a CTA, record steps) and all
+  // but the remainder of an even split elsewhere (measured on the GB300).
+  const bool wide = (T == 1 && prm.items >= 32 * grid) || a->record;
+  const int64_t ranged = static_cast<int64_t>(prm.items) * (wide ? 7 : 8) / 8;
+  prm.dyn0 = prm.sched ? static_cast<int>(ranged / grid) * grid : prm.items;
   const int pdl = a->use_pdl ? 1 : 0;
   const bool rec = a->record != 0;
   switch (T) {

@@ -51,7 +51,7 @@ class KdaArgs(ctypes.Structure):
         ("lower_bound", ctypes.c_float), ("scale", ctypes.c_float),
         ("eps", ctypes.c_float),
         ("err", _P), ("dbg", _P), ("path", ctypes.c_int32),
-        ("conv_f32", ctypes.c_int32),
+        ("conv_f32", ctypes.c_int32), ("sched", _P),
     ]
 
 

@@ -25,6 +25,7 @@ class KdaProbeArgs(ctypes.Structure):
         ("num_slots", ctypes.c_int32), ("stages", ctypes.c_int32),
         ("state", _P), ("slots", _P), ("err", _P),
         ("tokens", ctypes.c_int32), ("slot_cols", ctypes.c_int32), ("accepted", _P),
+        ("sched", _P),
     ]
 
 
@@ -64,12 +65,14 @@ def _check(name, t, dtype, shape=None):
 
 
 def kda_probe_page_copy(*, state, slots, accepted=None, tokens: int = 1, stages: int = 2,
-                        err=None, stream: Optional[torch.cuda.Stream] = None) -> None:
+                        err=None, sched=None,
+                        stream: Optional[torch.cuda.Stream] = None) -> None:
     """The step's page traffic with no arithmetic.  ``state`` float32
     [num_slots, heads, 128, 128]; decode (``tokens`` 1): ``slots`` int32
     [batch], every page read and written back in place; verify (``tokens``
     T > 1): ``slots`` int32 [batch, >= T] and ``accepted`` int32 [batch], the
-    page at slot ``slots[r, accepted[r]-1]`` written to each ``slots[r, t]``."""
+    page at slot ``slots[r, accepted[r]-1]`` written to each ``slots[r, t]``.
+    ``sched`` (int32 [2], zero): the step's schedule of shared items."""
     _check("state", state, torch.float32)
     if state.dim() != 4 or tuple(state.shape[2:]) != (128, 128):
         raise ValueError("state must be [num_slots, heads, 128, 128]")
@@ -86,7 +89,9 @@ def kda_probe_page_copy(*, state, slots, accepted=None, tokens: int = 1, stages:
             raise ValueError("slots must be [batch, >= tokens]")
         _check("accepted", accepted, torch.int32, (slots.shape[0],))
         cols = slots.shape[1]
-    for name, t in (("slots", slots), ("accepted", accepted), ("err", err)):
+    if sched is not None:
+        _check("sched", sched, torch.int32, (2,))
+    for name, t in (("slots", slots), ("accepted", accepted), ("err", err), ("sched", sched)):
         if t is not None and t.device != state.device:
             raise ValueError(f"{name} is on {t.device}, state on {state.device}")
     a = KdaProbeArgs()
@@ -96,6 +101,7 @@ def kda_probe_page_copy(*, state, slots, accepted=None, tokens: int = 1, stages:
     a.state, a.slots = state.data_ptr(), slots.data_ptr()
     a.accepted = accepted.data_ptr() if T > 1 else None
     a.err = err.data_ptr() if err is not None else None
+    a.sched = sched.data_ptr() if sched is not None else None
     with torch.cuda.device(state.device):
         s = stream if stream is not None else torch.cuda.current_stream(state.device)
         rc = call(a, s.cuda_stream)

@@ -85,8 +85,11 @@ def to_device(inputs: Dict[str, object], device="cuda") -> Dict[str, object]:
 
 
 def run_gpu(inputs: Dict[str, object], *, dbg: bool = True, reps: int = 1,
-            stream: Optional[torch.cuda.Stream] = None, path: int = 0) -> Dict[str, object]:
-    """One step of the CUDA library on a device copy of ``inputs``."""
+            stream: Optional[torch.cuda.Stream] = None, path: int = 0,
+            balance: bool = True) -> Dict[str, object]:
+    """One step of the CUDA library on a device copy of ``inputs`` (``balance``:
+    the step's own scheduler words, as the binding sets by default, or fixed
+    contiguous ranges only)."""
     d = to_device(inputs)
     B, H, T = d["batch"], d["heads"], d["tokens"]
     dev = torch.device("cuda")
@@ -99,7 +102,7 @@ def run_gpu(inputs: Dict[str, object], *, dbg: bool = True, reps: int = 1,
     dbgt = (torch.zeros((B, H, T, 4, 128), dtype=torch.bfloat16, device=dev)
             if dbg else None)
     step = step_from_inputs(d, out, rec_u=rec_u, rec_kg=rec_kg, err=err, dbg=dbgt,
-                            path=path)
+                            path=path, balance=balance)
     if stream is not None:
         stream.wait_stream(torch.cuda.current_stream())
     for _ in range(reps):

@@ -20,18 +20,23 @@ def _bits(t):
     return t.view(torch.int32)
 
 
+@pytest.mark.parametrize("shared", [False, True])
 @pytest.mark.parametrize("stages", [2, 3])
 @pytest.mark.parametrize("name", ["decode_b64_h32_pad8", "decode_b256_h32", "decode_b4_h8"])
-def test_pool_unchanged(name, stages):
+def test_pool_unchanged(name, stages, shared):
     w = WORKLOADS[name]
     inp = make_inputs(w)
     state = inp["state"].cuda()
     before = state.clone()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    kda_probe_page_copy(state=state, slots=inp["slots"].cuda(), stages=stages, err=err)
+    sched = torch.zeros(2, dtype=torch.int32, device="cuda") if shared else None
+    kda_probe_page_copy(state=state, slots=inp["slots"].cuda(), stages=stages, err=err,
+                        sched=sched)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert torch.equal(_bits(state), _bits(before))
+    if shared:
+        assert sched.tolist() == [0, 0]
 
 
 def test_out_of_pool_slot_flags_and_skips():
@@ -56,9 +61,10 @@ VERIFY = {
 }
 
 
+@pytest.mark.parametrize("shared", [False, True])
 @pytest.mark.parametrize("stages", [2, 3])
 @pytest.mark.parametrize("name", sorted(VERIFY))
-def test_verify_fanout(name, stages):
+def test_verify_fanout(name, stages, shared):
     w = VERIFY[name]
     inp = make_inputs(w)
     slots, acc, state = inp["slots"], inp["accepted"], inp["state"]
@@ -73,11 +79,14 @@ def test_verify_fanout(name, stages):
                 want[dst] = state[src]
     g = state.cuda()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sched = torch.zeros(2, dtype=torch.int32, device="cuda") if shared else None
     kda_probe_page_copy(state=g, slots=slots.cuda(), accepted=acc.cuda(), tokens=w.tokens,
-                        stages=stages, err=err)
+                        stages=stages, err=err, sched=sched)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert torch.equal(_bits(g.cpu()), _bits(want))
+    if shared:
+        assert sched.tolist() == [0, 0]
 
 
 def test_verify_errors_flag_and_skip():
