@@ -150,8 +150,11 @@ typedef struct kda_args {
   int32_t *sched;           /* optional i32 [2] device scheduler words, zero */
                             /* before first use; the kernel leaves them zero */
                             /* when it ends.  With them the persistent path  */
-                            /* hands the last eighth of the items out one at */
-                            /* a time to whichever CTA is free (same bits as */
+                            /* hands the items past the CTAs' contiguous     */
+                            /* ranges out one at a time to whichever CTA is  */
+                            /* free (an eighth of the items for decode with  */
+                            /* >= 32 items per SM and for record steps, else */
+                            /* the remainder of an even split; same bits as  */
                             /* without); NULL = fixed contiguous ranges.     */
                             /* Launches that may run at the same time (other */
                             /* streams, other threads) need separate words;  */
@@ -166,6 +169,16 @@ int kda_decode(const kda_args *args, void *stream);
 
 /* One speculative-verify step (tokens 2..8, record optional) on `stream`. */
 int kda_verify(const kda_args *args, void *stream);
+
+/* kda_decode (tokens == 1) or kda_verify (tokens > 1) with no caller
+ * allocation: args->sched is ignored and the library's own scheduler words
+ * (a static, zero-initialised device array per GPU, left zero by every
+ * launch) are used instead.  Every launch through this entry on one GPU
+ * shares those words, so such launches must not run at the same time: issue
+ * them in order on one stream (PDL chaining and graph capture are fine);
+ * concurrent streams or threads pass their own words to kda_decode /
+ * kda_verify.  Same return codes and bits as those calls. */
+int kda_step_noalloc(const kda_args *args, void *stream);
 
 /* Arguments of one record replay (kda_recover). */
 typedef struct kda_recover_args {

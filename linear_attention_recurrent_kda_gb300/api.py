@@ -62,6 +62,8 @@ class KdaStep:
     so its launches balance the last items over the CTAs; pass a tensor to
     share one between steps launched in order on one stream, or
     ``balance=False`` for fixed contiguous ranges only (same bits).
+    ``noalloc=True`` allocates nothing and calls ``kda_step_noalloc``, which
+    uses the library's own words (launches through it must be ordered).
     """
 
     def __init__(self, *, x, conv_weight, conv_state, f_a, f_b, beta, a_log,
@@ -70,7 +72,8 @@ class KdaStep:
                  tokens: int = 1, accepted=None, conv_bias=None,
                  gate_mode: int = 0, record: bool = False, rec_u=None,
                  rec_kg=None, err=None, dbg=None, use_pdl: bool = False,
-                 path: int = 0, sched=None, balance: bool = True):
+                 path: int = 0, sched=None, balance: bool = True,
+                 noalloc: bool = False):
         bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
         T = int(tokens)
         if not 1 <= T <= 8:
@@ -117,7 +120,9 @@ class KdaStep:
         _check("err", err, i32, allow_none=True)
         _check("dbg", dbg, bf, (B, H, T, 4, DK), allow_none=True)
         dev = output.device
-        if sched is None and balance:
+        if noalloc:
+            sched = None
+        elif sched is None and balance:
             sched = torch.zeros(2, dtype=i32, device=dev)
         _check("sched", sched, i32, (2,), allow_none=True)
         _same_device(dev, x=x, conv_weight=conv_weight, conv_bias=conv_bias,
@@ -145,7 +150,8 @@ class KdaStep:
         a.conv_f32 = int(conv_state.dtype == f32)
         a.sched = _ptr(sched)
         self.args = a
-        self.entry = "kda_decode" if T == 1 else "kda_verify"
+        self.entry = ("kda_step_noalloc" if noalloc else
+                      "kda_decode" if T == 1 else "kda_verify")
         self.device = dev
         # keep the tensors alive as long as the prepared step
         self._keep = (x, conv_weight, conv_state, f_a, f_b, beta, a_log, dt_bias,
@@ -183,7 +189,7 @@ INPUT_KEYS = ("x", "conv_weight", "conv_bias", "conv_state", "f_a", "f_b", "beta
 def step_from_inputs(dev_inputs: Dict[str, object], output: torch.Tensor, *,
                      rec_u=None, rec_kg=None, err=None, dbg=None,
                      use_pdl: bool = False, path: int = 0, sched=None,
-                     balance: bool = True) -> KdaStep:
+                     balance: bool = True, noalloc: bool = False) -> KdaStep:
     """A ``KdaStep`` from a device copy of a seeded workload's input dict."""
     d = dev_inputs
     T = int(d["tokens"])
@@ -197,7 +203,7 @@ def step_from_inputs(dev_inputs: Dict[str, object], output: torch.Tensor, *,
         conv_bias=d.get("conv_bias") if d.get("has_bias") else None,
         gate_mode=int(d["gate_mode"]), record=bool(d["record"]), rec_u=rec_u,
         rec_kg=rec_kg, err=err, dbg=dbg, use_pdl=use_pdl, path=path, sched=sched,
-        balance=balance)
+        balance=balance, noalloc=noalloc)
 
 
 def kda_recover(*, state, src_slots, dst_slots, accepted, rec_u, rec_kg, a_log,

@@ -1208,14 +1208,30 @@ static int launch_t(const Params &prm, const Layout &L, int dev, const DeviceFac
   return cudaGetLastError() == cudaSuccess ? KDA_SUCCESS : KDA_ERR_LAUNCH;
 }
 
+// The library's own scheduler words (kda_step_noalloc): a static device
+// array, zero at module load and left zero by every launch; its address on
+// the current GPU.
+static __device__ __align__(256) int32_t g_sched_words[64];
+
+static bool library_sched_words(int32_t **out) {
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_sched_words) != cudaSuccess) return false;
+  *out = static_cast<int32_t *>(p);
+  return true;
+}
+
 static bool aligned(const void *p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
 
-static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
+// own_sched: the library's scheduler words replace a->sched
+// (kda_step_noalloc; decode or verify by the token count).
+static int run_step(const kda_args *a, cudaStream_t stream, bool verify,
+                    bool own_sched = false) {
   if (!a) return KDA_ERR_NULL_ARGS;
   const int T = a->tokens;
   if (T < 1 || T > KDA_MAX_TOKENS) return KDA_ERR_TOKENS;
+  if (own_sched) verify = T > 1;
   if (verify ? T == 1 : T != 1) return KDA_ERR_TOKENS;
   if (a->gate_mode != 0 && a->gate_mode != 1) return KDA_ERR_GATE_MODE;
   if (a->record && T == 1) return KDA_ERR_RECORD;
@@ -1243,7 +1259,7 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
       (a->has_bias && !aligned(a->conv_bias, 2)) ||
       (a->rec_u && !aligned(a->rec_u, 4)) || (a->rec_kg && !aligned(a->rec_kg, 2)) ||
       (a->err && !aligned(a->err, 4)) || (a->dbg && !aligned(a->dbg, 2)) ||
-      (a->sched && !aligned(a->sched, 4)))
+      (!own_sched && a->sched && !aligned(a->sched, 4)))
     return KDA_ERR_ALIGNMENT;
 
   int dev = 0;
@@ -1264,6 +1280,7 @@ static int run_step(const kda_args *a, cudaStream_t stream, bool verify) {
   prm.items = a->batch * a->heads;
   prm.stages = L.stages;
   prm.sched = a->sched;
+  if (own_sched && !library_sched_words(&prm.sched)) return KDA_ERR_DEVICE;
   prm.stage_bytes = L.stage_bytes;
   prm.conv_off = L.conv_off;
   prm.x_off = L.x_off;
@@ -1348,6 +1365,10 @@ int kda_decode(const kda_args *args, void *stream) {
 
 int kda_verify(const kda_args *args, void *stream) {
   return kda::run_step(args, static_cast<cudaStream_t>(stream), true);
+}
+
+int kda_step_noalloc(const kda_args *args, void *stream) {
+  return kda::run_step(args, static_cast<cudaStream_t>(stream), false, true);
 }
 
 const char *kda_strerror(int code) {

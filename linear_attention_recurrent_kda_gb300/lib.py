@@ -31,7 +31,7 @@ KDA_DEVERR_SLOT = 1
 KDA_DEVERR_ACCEPTED = 2
 KDA_DEVERR_TIMEOUT = 4
 
-EXPORTED = ("kda_decode", "kda_verify", "kda_recover", "kda_oproj",
+EXPORTED = ("kda_decode", "kda_verify", "kda_step_noalloc", "kda_recover", "kda_oproj",
             "kda_selftest_wait_timeout", "kda_strerror", "kda_abi_version")
 
 
@@ -98,7 +98,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     if not os.path.exists(p):
         raise ImportError(f"KDA CUDA library not found at {p}")
     lib = ctypes.CDLL(p)
-    for name in ("kda_decode", "kda_verify"):
+    for name in ("kda_decode", "kda_verify", "kda_step_noalloc"):
         fn = getattr(lib, name)
         fn.argtypes = [ctypes.POINTER(KdaArgs), ctypes.c_void_p]
         fn.restype = ctypes.c_int

@@ -86,10 +86,11 @@ def to_device(inputs: Dict[str, object], device="cuda") -> Dict[str, object]:
 
 def run_gpu(inputs: Dict[str, object], *, dbg: bool = True, reps: int = 1,
             stream: Optional[torch.cuda.Stream] = None, path: int = 0,
-            balance: bool = True) -> Dict[str, object]:
+            balance: bool = True, noalloc: bool = False) -> Dict[str, object]:
     """One step of the CUDA library on a device copy of ``inputs`` (``balance``:
     the step's own scheduler words, as the binding sets by default, or fixed
-    contiguous ranges only)."""
+    contiguous ranges only; ``noalloc``: through kda_step_noalloc, the
+    library's own words)."""
     d = to_device(inputs)
     B, H, T = d["batch"], d["heads"], d["tokens"]
     dev = torch.device("cuda")
@@ -102,7 +103,7 @@ def run_gpu(inputs: Dict[str, object], *, dbg: bool = True, reps: int = 1,
     dbgt = (torch.zeros((B, H, T, 4, 128), dtype=torch.bfloat16, device=dev)
             if dbg else None)
     step = step_from_inputs(d, out, rec_u=rec_u, rec_kg=rec_kg, err=err, dbg=dbgt,
-                            path=path, balance=balance)
+                            path=path, balance=balance, noalloc=noalloc)
     if stream is not None:
         stream.wait_stream(torch.cuda.current_stream())
     for _ in range(reps):

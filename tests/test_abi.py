@@ -68,6 +68,7 @@ def test_null_args():
     lib = kl.load()
     assert lib.kda_decode(None, None) == kl.KDA_ERR_NULL_ARGS
     assert lib.kda_verify(None, None) == kl.KDA_ERR_NULL_ARGS
+    assert lib.kda_step_noalloc(None, None) == kl.KDA_ERR_NULL_ARGS
 
 
 @pytest.mark.parametrize("entry,kw,code", [
@@ -84,6 +85,16 @@ def test_null_args():
     ("kda_verify", dict(tokens=3, slot_cols=2, conv_width=5), kl.KDA_ERR_SHAPE),
     ("kda_decode", dict(conv_width=2), kl.KDA_ERR_CONV_WIDTH),
     ("kda_decode", {}, kl.KDA_ERR_NULL_POINTER),
+    # the no-allocation entry validates exactly as kda_decode / kda_verify
+    # (chosen by the token count) before it touches the library's words
+    ("kda_step_noalloc", dict(tokens=0), kl.KDA_ERR_TOKENS),
+    ("kda_step_noalloc", dict(tokens=9), kl.KDA_ERR_TOKENS),
+    ("kda_step_noalloc", dict(gate_mode=3), kl.KDA_ERR_GATE_MODE),
+    ("kda_step_noalloc", dict(record=1), kl.KDA_ERR_RECORD),
+    ("kda_step_noalloc", dict(batch=0), kl.KDA_SUCCESS),
+    ("kda_step_noalloc", dict(tokens=3, slot_cols=2, conv_width=5), kl.KDA_ERR_SHAPE),
+    ("kda_step_noalloc", dict(tokens=4, conv_width=5, slot_cols=4), kl.KDA_ERR_CONV_WIDTH),
+    ("kda_step_noalloc", {}, kl.KDA_ERR_NULL_POINTER),
 ])
 def test_host_validation_without_gpu(entry, kw, code):
     assert kl.call(entry, _args(**kw), 0) == code
@@ -96,6 +107,10 @@ def test_alignment_rule_checked_before_any_device_call():
                  "a_log", "dt_bias", "slots", "conv_state", "state", "output"):
         setattr(a, name, fake)
     a.state = fake + 4            # FP32 pool must be 16-byte aligned
+    assert kl.call("kda_decode", a, 0) == kl.KDA_ERR_ALIGNMENT
+    assert kl.call("kda_step_noalloc", a, 0) == kl.KDA_ERR_ALIGNMENT
+    a.state = fake
+    a.sched = fake + 2            # scheduler words must be 4-byte aligned
     assert kl.call("kda_decode", a, 0) == kl.KDA_ERR_ALIGNMENT
 
 

@@ -6,7 +6,8 @@ first; without them every item sits in a fixed contiguous range.  Items are
 independent, so both must give the same bits on every output, pool, record
 and the error word, and the words must be back at zero after every launch
 (the last CTA zeroes them).  The oracle comparisons of the other GPU tests
-run with the binding's default words; these tests pin the schedule itself.
+run with the binding's default words; these tests pin the schedule itself,
+and kda_step_noalloc, the same step on the library's own static words.
 """
 from __future__ import annotations
 
@@ -140,3 +141,46 @@ def test_graph_replays_share_words():
     for a, b in zip(got, [out, d["state"], d["conv_state"]]):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
     assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c.name + f"_t{c.tokens}" for c in CASES])
+def test_noalloc_entry_same_bits(w):
+    """kda_step_noalloc (the library's own words) gives the fixed-range bits,
+    twice in a row (the first launch left the words at zero)."""
+    inp = make_inputs(w)
+    fixed = run_gpu(inp, dbg=False, balance=False, path=kl.KDA_PATH_PERSISTENT)
+    for _ in range(2):
+        own = run_gpu(inp, dbg=False, noalloc=True, path=kl.KDA_PATH_PERSISTENT)
+        same_bits(own, fixed)
+
+
+def test_noalloc_entry_repeated_launches_and_oracle():
+    """Thirty launches through kda_step_noalloc on one stream, pools restored
+    before each, reproduce the first launch's bits; one more from the seeded
+    pools matches the oracle (its items all ran: a word left non-zero would
+    hand out no shared items)."""
+    w = wl(seed=618, batch=200, heads=6, num_slots=256, pad=11)
+    d = to_device(make_inputs(w))
+    B, H, T = d["batch"], d["heads"], d["tokens"]
+    out = torch.full((B * T, H * 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dbgt = torch.zeros((B, H, T, 4, 128), dtype=torch.bfloat16, device="cuda")
+    step = step_from_inputs(d, out, err=err, dbg=dbgt, noalloc=True,
+                            path=kl.KDA_PATH_PERSISTENT)
+    st0, cv0 = d["state"].clone(), d["conv_state"].clone()
+    ref = None
+    for _ in range(30):
+        d["state"].copy_(st0)
+        d["conv_state"].copy_(cv0)
+        out.fill_(float("nan"))
+        step()
+        cur = [out.clone(), d["state"].clone(), d["conv_state"].clone()]
+        if ref is None:
+            ref = cur
+        else:
+            for a, b in zip(cur, ref):
+                assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    torch.cuda.synchronize()
+    gpu = {"output": bits(out), "state": d["state"].cpu().numpy(),
+           "conv_state": bits(d["conv_state"]), "err": int(err.item()), "dbg": bits(dbgt)}
+    compare(make_inputs(w), gpu)
