@@ -242,10 +242,12 @@ def run_recover(args):
     acc = torch.randint(1, T + 1, (B,), generator=torch.Generator().manual_seed(3),
                         dtype=torch.int32).to(dev)
 
+    sched = torch.zeros(2, dtype=torch.int32, device=dev)
+
     def call():
         kda_recover(state=d["state"], src_slots=src, dst_slots=src, accepted=acc,
                     rec_u=ru, rec_kg=rk, a_log=d["a_log"], dt_bias=d["dt_bias"],
-                    lower_bound=w.lower_bound)
+                    lower_bound=w.lower_bound, sched=sched)
 
     for _ in range(max(args.warmup, 3)):
         call()

@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 6
+#define KDA_ABI_VERSION 7
 #define KDA_DK 128
 #define KDA_MAX_TOKENS 8
 
@@ -197,6 +197,10 @@ typedef struct kda_recover_args {
   float lower_bound;        /* as in the step that wrote the records           */
   float *state;             /* f32 [num_slots, H, 128, 128]       in/out       */
   int32_t *err;             /* optional device word for KDA_DEVERR_* flags     */
+  int32_t *sched;           /* optional i32 [2] scheduler words, as in         */
+                            /* kda_args (zero before first use, left zero;     */
+                            /* concurrent launches need their own); NULL =     */
+                            /* contiguous item ranges only.  Same bits.        */
 } kda_recover_args;
 
 /* Record replay ("RecoverSSM" on the page, referenced but not shown there).

@@ -207,10 +207,12 @@ def step_from_inputs(dev_inputs: Dict[str, object], output: torch.Tensor, *,
 
 
 def kda_recover(*, state, src_slots, dst_slots, accepted, rec_u, rec_kg, a_log,
-                dt_bias, lower_bound: float, err=None,
+                dt_bias, lower_bound: float, err=None, sched=None, balance: bool = True,
                 stream: Optional[torch.cuda.Stream] = None) -> None:
     """Record replay (include/kda.h ``kda_recover``): rebuild the accepted
-    state pages from checkpoint pages and a record-mode verify's records."""
+    state pages from checkpoint pages and a record-mode verify's records.
+    ``sched``: scheduler words (int32 [2], zero); by default a fresh pair per
+    call (``balance=False``: contiguous item ranges only, same bits)."""
     bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
     _check("rec_u", rec_u, f32)
     if rec_u.dim() != 4 or rec_u.shape[3] != DK:
@@ -226,8 +228,12 @@ def kda_recover(*, state, src_slots, dst_slots, accepted, rec_u, rec_kg, a_log,
     _check("a_log", a_log, f32, (H,))
     _check("dt_bias", dt_bias, f32, (H * DK,))
     _check("err", err, i32, allow_none=True)
+    if sched is None and balance:
+        sched = torch.zeros(2, dtype=i32, device=state.device)
+    _check("sched", sched, i32, (2,), allow_none=True)
     _same_device(state.device, src_slots=src_slots, dst_slots=dst_slots, accepted=accepted,
-                 rec_u=rec_u, rec_kg=rec_kg, a_log=a_log, dt_bias=dt_bias, err=err)
+                 rec_u=rec_u, rec_kg=rec_kg, a_log=a_log, dt_bias=dt_bias, err=err,
+                 sched=sched)
     a = _lib.KdaRecoverArgs()
     a.batch, a.heads, a.tokens, a.num_slots = B, H, T, state.shape[0]
     a.src_slots, a.dst_slots, a.accepted = (_ptr(src_slots), _ptr(dst_slots),
@@ -236,6 +242,7 @@ def kda_recover(*, state, src_slots, dst_slots, accepted, rec_u, rec_kg, a_log,
     a.a_log, a.dt_bias = _ptr(a_log), _ptr(dt_bias)
     a.lower_bound = float(lower_bound)
     a.state, a.err = _ptr(state), _ptr(err)
+    a.sched = _ptr(sched)
     with torch.cuda.device(state.device):
         s = stream if stream is not None else torch.cuda.current_stream(state.device)
         rc = _lib.call("kda_recover", a, s.cuda_stream)

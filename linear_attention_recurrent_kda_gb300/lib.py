@@ -62,7 +62,7 @@ class KdaRecoverArgs(ctypes.Structure):
         ("tokens", ctypes.c_int32), ("num_slots", ctypes.c_int32),
         ("src_slots", _P), ("dst_slots", _P), ("accepted", _P),
         ("rec_u", _P), ("rec_kg", _P), ("a_log", _P), ("dt_bias", _P),
-        ("lower_bound", ctypes.c_float), ("state", _P), ("err", _P),
+        ("lower_bound", ctypes.c_float), ("state", _P), ("err", _P), ("sched", _P),
     ]
 
 

@@ -49,7 +49,7 @@ def test_probe_library_exports_its_header():
 
 
 def test_version_and_strerror():
-    assert kl.load().kda_abi_version() == 6
+    assert kl.load().kda_abi_version() == 7
     for code in range(0, 12):
         assert kl.strerror(code)
     assert "unknown" in kl.strerror(999)

@@ -180,3 +180,36 @@ def test_replay_full_size_record_workload_sampled():
             continue
         g, t = got[dst[r]].astype(np.float64), want[dst[r]]
         assert np.all(np.abs(g - t) <= STATE_ATOL + STATE_RTOL * np.abs(t)), r
+
+
+@pytest.mark.parametrize("full", [False, True])
+def test_replay_shared_items_same_bits_as_fixed_ranges(full):
+    """The replay with scheduler words (the items past the CTAs' ranges handed
+    out one at a time) writes the same pages bit for bit as with contiguous
+    ranges only, and leaves the words at zero; 96 requests x 8 heads (768
+    items over at most one CTA per SM) and the full record workload."""
+    w = (WORKLOADS["verify_q8_record_b64_h64"] if full else
+         Workload(name="rs", batch=96, heads=8, tokens=6, num_slots=97, conv_width=8,
+                  slot_layout="checkpoint", record=True, pad=9, seed=771))
+    inp = make_inputs(w)
+    o = to_oracle(inp)
+    d_rec, ru, rk, _ = run_step(inp, record=True)
+    B, H, T = w.batch, w.heads, w.tokens
+    src = torch.from_numpy(src_slots(o)).cuda()
+    dst = torch.arange(w.num_slots, w.num_slots + B, dtype=torch.int32, device="cuda")
+    acc = torch.from_numpy(np.random.default_rng(12).integers(0, T + 1, size=B)
+                           .astype(np.int32)).cuda()
+    base = torch.cat([d_rec["state"], torch.zeros((B, H, 128, 128), device="cuda")])
+    outs = []
+    sched = torch.zeros(2, dtype=torch.int32, device="cuda")
+    for kw in (dict(balance=False), dict(sched=sched), dict(sched=sched)):
+        st = base.clone()
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kda_recover(state=st, src_slots=src, dst_slots=dst, accepted=acc, rec_u=ru,
+                    rec_kg=rk, a_log=d_rec["a_log"], dt_bias=d_rec["dt_bias"],
+                    lower_bound=w.lower_bound, err=err, **kw)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs.append(st.view(torch.int32).cpu())
+    assert sched.tolist() == [0, 0]
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
