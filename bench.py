@@ -41,6 +41,8 @@ KERNEL_SOURCE = os.path.join(ROOT, "linear_attention_recurrent_kda_gb300", "csrc
                              "kda_step.cu")
 OPROJ_SOURCE = os.path.join(ROOT, "linear_attention_recurrent_kda_gb300", "csrc",
                             "kda_oproj.cu")
+RECOVER_SOURCE = os.path.join(ROOT, "linear_attention_recurrent_kda_gb300", "csrc",
+                              "kda_recover.cu")
 
 
 def dist_env():
@@ -271,6 +273,7 @@ def run_recover(args):
                                         "replayed_tokens": acc_live},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                      "frac": gbs / peak, "peak_source": f"{kind} hbm_gbs",
+                     "traffic": ncu_traffic(name, "kda_recover", RECOVER_SOURCE),
                      "algorithmic_bytes_per_launch": nbytes}}), flush=True)
 
 

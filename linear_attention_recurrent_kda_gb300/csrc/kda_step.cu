@@ -9,9 +9,13 @@
 //   * Persistent kernel, one CTA of four warpgroups per SM.  Each CTA owns a
 //     contiguous range of items in head-major order (item = h * batch + r), so
 //     the per-head f_b tensor-core fragments stay in registers across its
-//     items.
+//     items; with scheduler words the items past the ranges then go one at a
+//     time to whichever CTA's producer asks first (an atomic counter the last
+//     CTA zeroes), so CTAs on slower SMs or with slower pages take fewer and
+//     the CTAs finish together.
 //   * Three warp roles work on consecutive items at the same time:
-//       producer   (warpgroup 3, one thread): per item resolves the slots,
+//       producer   (warpgroup 3, one thread): picks the next item (its
+//                  range, then shared items, then an end marker), resolves the slots,
 //                  loads beta and the write targets into an item descriptor and
 //                  stages the 64 KiB FP32 state page plus the item's conv rows,
 //                  x, gate and f_a rows into a 2-3 stage shared-memory ring

@@ -1,8 +1,10 @@
 """The persistent kernel's item schedule: contiguous ranges, then shared items.
 
-With scheduler words (kda_args.sched) each CTA walks a contiguous 7/8 of its
-even share and the remaining items go one at a time to whichever CTA asks
-first; without them every item sits in a fixed contiguous range.  Items are
+With scheduler words (kda_args.sched) each CTA walks a contiguous range (7/8
+of its even share for decode with many items per CTA and for record steps,
+else all but the remainder of an even split) and the remaining items go one
+at a time to whichever CTA asks first; without them every item sits in a
+fixed contiguous range.  Items are
 independent, so both must give the same bits on every output, pool, record
 and the error word, and the words must be back at zero after every launch
 (the last CTA zeroes them).  The oracle comparisons of the other GPU tests
