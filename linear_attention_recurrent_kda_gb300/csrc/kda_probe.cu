@@ -5,8 +5,9 @@
 // read by one TMA bulk copy into a shared-memory stage and written by bulk
 // stores to every page the step writes (decode: back in place; verify: the
 // slots of the T tokens): the bytes and the order of the step (persistent
-// CTAs, one per SM, over contiguous item ranges, a ring of `stages` pages per
-// CTA), with no conv, gate, recurrence or epilogue.  Its bandwidth is the
+// CTAs, one per SM, over contiguous item ranges and, with scheduler words,
+// the step's shared items; a ring of `stages` pages per CTA), with no conv,
+// gate, recurrence or epilogue.  Its bandwidth is the
 // ceiling that the step's own page traffic can reach on this memory system.
 // One thread per CTA issues everything.
 #include <cuda_runtime.h>
