@@ -1,10 +1,12 @@
 """Repeated launches from restored pools reproduce the first launch's bits.
 
 Each workload runs 300 times (KDA_SOAK_LAUNCHES overrides the count for a
-longer run); before every launch the state and conv pools
-are restored and the outputs and records are filled with NaN, so any
-launch-to-launch difference (a race between the kernel's roles, a stale
-stage, a missed barrier) shows up as changed bits."""
+longer run), through the binding's default call (its own scheduler words)
+and through kda_step_noalloc (the library's static words); before every
+launch the state and conv pools are restored and the outputs and records
+are filled with NaN, so any launch-to-launch difference (a race between the
+kernel's roles, a stale stage, a missed barrier, scheduler words not back at
+zero) shows up as changed bits."""
 from __future__ import annotations
 
 import os
@@ -24,8 +26,9 @@ def _bits(t):
     return t.view(torch.uint8) if t.element_size() != 4 or t.dtype != torch.int32 else t
 
 
+@pytest.mark.parametrize("noalloc", [False, True], ids=["own_words", "noalloc"])
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
-def test_repeated_launches_are_bit_stable(name):
+def test_repeated_launches_are_bit_stable(name, noalloc):
     w = WORKLOADS[name]
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in make_inputs(w).items()}
     B, H, T = w.batch, w.heads, w.tokens
@@ -36,7 +39,7 @@ def test_repeated_launches_are_bit_stable(name):
         ru = torch.empty((B, H, T, 128), dtype=torch.float32, device="cuda")
         rk = torch.empty((B, H, T, 256), dtype=torch.bfloat16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    step = step_from_inputs(d, out, rec_u=ru, rec_kg=rk, err=err)
+    step = step_from_inputs(d, out, rec_u=ru, rec_kg=rk, err=err, noalloc=noalloc)
     ref = None
     differing = torch.zeros((), dtype=torch.int64, device="cuda")
     for _ in range(N):
