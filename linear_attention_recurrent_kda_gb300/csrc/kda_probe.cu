@@ -88,12 +88,13 @@ __global__ void __launch_bounds__(32) page_copy_kernel(const __grid_constant__ k
     for (; n < n1; ++n)
       if (probe_resolve(a, n, it)) return n++;
     while (!drained) {
-      const int m = dyn0 + atomicAdd(a.sched, 1);
+      // 64-bit, the counter read unsigned: no wrap however many items there are.
+      const int64_t m = dyn0 + static_cast<int64_t>(static_cast<uint32_t>(atomicAdd(a.sched, 1)));
       if (m >= items) {
         drained = true;
         break;
       }
-      if (probe_resolve(a, m, it)) return m;
+      if (probe_resolve(a, static_cast<int>(m), it)) return static_cast<int>(m);
     }
     return -1;
   };

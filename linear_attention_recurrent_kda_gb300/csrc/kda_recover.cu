@@ -136,10 +136,13 @@ __device__ void producer(const Params &p, uint8_t *smem, Ctrl *ctl, Desc *desc,
     // The CTA's k-th item: its own range, then shared items.
     int n = n0 + k < n1 ? n0 + k : -1;
     if (n < 0 && !drained) {
-      n = p.dyn0 + atomicAdd(p.sched, 1);
-      if (n >= p.items) {
+      // 64-bit, the counter read unsigned: no wrap however many items there are.
+      const int64_t m =
+          p.dyn0 + static_cast<int64_t>(static_cast<uint32_t>(atomicAdd(p.sched, 1)));
+      if (m >= p.items) {
         drained = true;
-        n = -1;
+      } else {
+        n = static_cast<int>(m);
       }
     }
     Desc &d = desc[stage];

@@ -268,8 +268,9 @@ __device__ void producer_role(const Params &p, uint8_t *smem, Ctrl *ctl,
   auto item_at = [&](int k) -> int {
     if (n0 + k < n1) return n0 + k;
     if (drained) return -1;
-    const int n = p.dyn0 + atomicAdd(p.sched, 1);
-    if (n < p.items) return n;
+    // 64-bit, the counter read unsigned: no wrap however many items there are.
+    const int64_t n = p.dyn0 + static_cast<int64_t>(static_cast<uint32_t>(atomicAdd(p.sched, 1)));
+    if (n < p.items) return static_cast<int>(n);
     drained = true;
     return -1;
   };
